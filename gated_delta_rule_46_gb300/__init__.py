@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) Kimi Delta Attention: gate, chunkwise prefill, decode step.
+
+The compute path is the CUDA library built from ``csrc/`` (C ABI in
+``include/kda.h``); ``kda`` is its thin ctypes binding and ``inputs`` the
+seeded synthetic workloads.
+"""
+from . import inputs  # noqa: F401
+from .kda import (KDAError, chunk_prefill, check_device_status, decode_step, gate,  # noqa: F401
+                  lib, library_path, workspace_size)
+
+__all__ = ["inputs", "KDAError", "chunk_prefill", "check_device_status", "decode_step", "gate",
+           "lib", "library_path", "workspace_size"]

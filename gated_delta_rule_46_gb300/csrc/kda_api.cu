@@ -1,0 +1,135 @@
+// kda_api.cu -- the extern "C" entry points declared in include/kda.h:
+// argument validation on the host, kernel selection, launches on the caller's
+// stream, and the device status word.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_gate(const void *z, bool bf16, const float *A, float *g, int64_t n_tokens,
+                        int H, int dk, cudaStream_t st);
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *z,
+                          const float *A, const float *beta, float *state, void *out, int N,
+                          int H, int dk, int dv, bool bf16, cudaStream_t st);
+cudaError_t launch_prefill_serial(const void *q, const void *k, const void *v, const void *z,
+                                  const float *A, const float *beta, const int32_t *cu,
+                                  int num_seqs, int64_t total, int H, int dk, int dv, bool bf16,
+                                  const float *s0, float *s1, void *out, uint32_t *status,
+                                  cudaStream_t st);
+cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
+                              const float *A, const float *beta, const int32_t *cu,
+                              int num_seqs, int64_t total, int H, const float *s0, float *s1,
+                              void *out, void *workspace, cudaStream_t st);
+}  // namespace kda
+
+namespace {
+
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
+
+kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+// The tensor-core prefill covers bf16 with dk = dv = 128 and needs 16-byte
+// aligned q/k/v/z for its TMA descriptors.
+bool use_tc(kda_dtype_t dt, int dk, int dv, const void *q, const void *k, const void *v,
+            const void *z, int64_t total) {
+    return dt == KDA_BF16 && dk == 128 && dv == 128 && total > 0 && total < (int64_t(1) << 31) &&
+           aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(z, 16);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(kda_status_t status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported shape or dtype";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA call or launch failed";
+        case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT: device-side wait expired";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+kda_status_t kda_gate(const void *z, kda_dtype_t z_dtype, const float *A, float *g_out,
+                      int64_t n_tokens, int H, int dk, kda_stream_t stream) {
+    if (n_tokens < 0 || H <= 0 || dk <= 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(z_dtype)) return KDA_ERR_UNSUPPORTED;
+    if (!dim_ok(dk)) return KDA_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return KDA_OK;
+    if (!z || !A || !g_out) return KDA_ERR_INVALID_ARG;
+    if (!aligned(z, 16) || !aligned(g_out, 16)) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_gate(z, z_dtype == KDA_BF16, A, g_out, n_tokens, H, dk,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                  kda_dtype_t dtype) {
+    (void)total_tokens; (void)H; (void)dk; (void)dv; (void)dtype;
+    if (num_seqs < 0) num_seqs = 0;
+    size_t bytes = kda::kWsOrder + sizeof(int32_t) * (size_t)num_seqs;
+    return (bytes + 255) & ~size_t(255);
+}
+
+kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,
+                               const float *A, const float *beta, const int32_t *cu_seqlens,
+                               int num_seqs, int64_t total_tokens, int H, int dk, int dv,
+                               kda_dtype_t dtype, const float *initial_state,
+                               float *final_state, void *out, void *workspace,
+                               size_t workspace_bytes, kda_stream_t stream) {
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || dk <= 0 || dv <= 0)
+        return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens >= (int64_t(1) << 31) || (int64_t)num_seqs * H >= (int64_t(1) << 31))
+        return KDA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 16) ||
+        workspace_bytes < kda_prefill_workspace_size(total_tokens, num_seqs, H, dk, dv, dtype))
+        return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens || !A) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !z || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (use_tc(dtype, dk, dv, q, k, v, z, total_tokens)) {
+        return from_cuda(kda::launch_prefill_tc(q, k, v, z, A, beta, cu_seqlens, num_seqs,
+                                                total_tokens, H, initial_state, final_state, out,
+                                                workspace, st));
+    }
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws + kda::kWsStatus);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    return from_cuda(kda::launch_prefill_serial(q, k, v, z, A, beta, cu_seqlens, num_seqs,
+                                                total_tokens, H, dk, dv, dtype == KDA_BF16,
+                                                initial_state, final_state, out, status, st));
+}
+
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const void *z,
+                             const float *A, const float *beta, float *state, void *out,
+                             int N, int H, int dk, int dv, kda_dtype_t dtype,
+                             kda_stream_t stream) {
+    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H >= (int64_t(1) << 31)) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !z || !A || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned(state, 16)) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_decode(q, k, v, z, A, beta, state, out, N, H, dk, dv,
+                                        dtype == KDA_BF16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status_t kda_check_device_status(const void *workspace, kda_stream_t stream) {
+    if (!workspace) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, static_cast<const uint8_t *>(workspace) + kda::kWsStatus,
+                        sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+    return static_cast<kda_status_t>(word);
+}
+
+}  // extern "C"

@@ -26,7 +26,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-SLAB = 65536
+SLAB = 16384
 
 # tensor ids for the per-stream seeds
 _Q, _K, _V, _Z, _BETA, _A, _STATE, _LENS = 1, 2, 3, 4, 5, 6, 7, 8

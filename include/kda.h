@@ -1,0 +1,144 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * Kimi Delta Attention (KDA) is the recurrent sequence mixer of the Kimi K3
+ * hybrid stack ("Kimi K3 internals analysis", molayo1419.me, section
+ * "Sequence mixing"): a fixed-size per-head state S (dk x dv, rows = key
+ * channels) replaces the KV cache and is written by the delta rule, after a
+ * channel-wise retention factor has decayed the old state:
+ *
+ *     g_t   = g_min * sigmoid(exp(A) * z_t),  g_min = -5,  alpha_t = exp(g_t)
+ *     S'    = Diag(alpha_t) S_{t-1}
+ *     S_t   = S' + beta_t k_t (v_t - S'^T k_t)^T
+ *     o_t   = S_t^T q_t
+ *
+ * The bounded gate keeps the cumulative log-decay of any 16 consecutive tokens
+ * inside (-80, 0) (same section), which is what lets the chunked prefill use
+ * dense tensor-core tiles on the diagonal blocks too.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers, allocated and owned by the
+ *     caller.  The library allocates no device memory in any call.
+ *   - Every call is asynchronous on the caller's stream `stream` (0 = the
+ *     legacy default stream).  Argument errors are detected on the host,
+ *     before anything is launched, and returned as KDA_ERR_INVALID_ARG or
+ *     KDA_ERR_UNSUPPORTED; nothing is written in that case.  A failed launch
+ *     returns KDA_ERR_CUDA.  Conditions found on the device (a bounded wait
+ *     that expired) are recorded in a status word inside the caller's
+ *     workspace and read with kda_check_device_status().  No call traps.
+ *   - Layouts are dense row-major ("packed"): tokens of all sequences are
+ *     concatenated along the first axis, sequence i owning rows
+ *     [cu_seqlens[i], cu_seqlens[i+1]).  Per-token tensors are [T, H, d].
+ *   - q and k are used as given (callers normalise them; there is no 1/sqrt(dk)
+ *     scale).  beta is a scalar per (token, head), already in (0, 1).
+ *   - A, beta, g and every state are float32.  q, k, v, z and the output share
+ *     one element type, kda_dtype_t.
+ *   - Supported head dimensions: dk, dv in {32, 64, 128}.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t / CUstream). */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, misaligned buffer */
+    KDA_ERR_UNSUPPORTED = 2,    /* valid but unsupported shape or dtype */
+    KDA_ERR_CUDA = 3,           /* a CUDA runtime/driver call or launch failed */
+    KDA_ERR_DEVICE_TIMEOUT = 4  /* a device-side bounded wait expired */
+} kda_status_t;
+
+typedef enum {
+    KDA_F32 = 0,
+    KDA_BF16 = 1
+} kda_dtype_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kda_status_string(kda_status_t status);
+
+/*
+ * kda_gate -- the bounded gate ("Sequence mixing": g = g_min * sigmoid(exp(A) z),
+ * g_min = -5).
+ *   z      [n_tokens, H, dk], element type z_dtype
+ *   A      [H, dk] float32
+ *   g_out  [n_tokens, H, dk] float32 (written)
+ * g_out lies in [-5, 0): in float32 the sigmoid rounds to exactly 1 once
+ * exp(A) z exceeds about 16.6, so the open bound of the exact formula closes.
+ */
+kda_status_t kda_gate(const void *z, kda_dtype_t z_dtype, const float *A, float *g_out,
+                      int64_t n_tokens, int H, int dk, kda_stream_t stream);
+
+/*
+ * kda_prefill_workspace_size -- bytes of device workspace kda_chunk_prefill
+ * needs for these sizes (a few KB: a status word, a work counter and a
+ * schedule of num_seqs entries).  The workspace holds no data between calls
+ * except the status word, which kda_chunk_prefill clears on entry.
+ */
+size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                  kda_dtype_t dtype);
+
+/*
+ * kda_chunk_prefill -- KDA over a packed batch of variable-length sequences
+ * ("Sequence mixing"; the state is the fixed-size memory of the same section).
+ *   q, k, z        [total_tokens, H, dk], element type dtype
+ *   v              [total_tokens, H, dv], element type dtype
+ *   A              [H, dk] float32
+ *   beta           [total_tokens, H] float32
+ *   cu_seqlens     [num_seqs + 1] int32, device; cu_seqlens[0] = 0, non-decreasing,
+ *                  cu_seqlens[num_seqs] = total_tokens (not checked on the host:
+ *                  reading it would synchronise)
+ *   initial_state  [num_seqs, H, dk, dv] float32, or NULL for zeros
+ *   final_state    [num_seqs, H, dk, dv] float32 (written), or NULL; it may be
+ *                  the same buffer as initial_state
+ *   out            [total_tokens, H, dv], element type dtype (written)
+ *   workspace      device buffer of at least kda_prefill_workspace_size() bytes,
+ *                  16-byte aligned
+ * Length-0 sequences copy their initial state (or zeros) to final_state.
+ * bf16 inputs with dk = dv = 128 run the chunkwise tensor-core kernel (64-token
+ * chunks, 16-token decay tiles); every other supported case runs the
+ * token-serial float32 kernel.
+ */
+kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,
+                               const float *A, const float *beta, const int32_t *cu_seqlens,
+                               int num_seqs, int64_t total_tokens, int H, int dk, int dv,
+                               kda_dtype_t dtype, const float *initial_state,
+                               float *final_state, void *out, void *workspace,
+                               size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_decode_step -- one new token for each of N sequences; the recurrent
+ * state is read and updated IN PLACE (the fixed-size state that replaces the
+ * KV cache, "Sequence mixing").
+ *   q, k, z   [N, H, dk], element type dtype
+ *   v         [N, H, dv], element type dtype
+ *   A         [H, dk] float32
+ *   beta      [N, H] float32
+ *   state     [N, H, dk, dv] float32, read and overwritten
+ *   out       [N, H, dv], element type dtype (written)
+ */
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const void *z,
+                             const float *A, const float *beta, float *state, void *out,
+                             int N, int H, int dk, int dv, kda_dtype_t dtype,
+                             kda_stream_t stream);
+
+/*
+ * kda_check_device_status -- synchronises `stream`, reads the status word that
+ * kda_chunk_prefill keeps in `workspace`, and returns KDA_OK or the recorded
+ * device-side error (KDA_ERR_DEVICE_TIMEOUT).  Returns KDA_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+kda_status_t kda_check_device_status(const void *workspace, kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */
