@@ -1,0 +1,400 @@
+"""Benchmark of the KDA hot path on GB300: prefill tokens/s and decode tokens/s.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * an L2 flush (a 256 MB write, larger than the 129 MB L2; the prefill
+    inputs of this workload would otherwise stay cached between steps),
+  * one kda_chunk_prefill over the 4096-token prefill workload
+    (B=1, H=16, dk=dv=128, bf16, float32 initial state 0.1*N(0,1)),
+  * 128 consecutive kda_decode_step calls over the decode workload
+    (256 sequences, H=32, dk=dv=128, bf16 inputs, 537 MB float32 state,
+    read and written in place every step; the state is larger than L2).
+`value` is prefill tokens/s (tokens of the sequence per second of device time
+of the prefill calls); `decode.value` is decode tokens/s (sequences x steps per
+second of device time of the decode calls).  `e2e` repeats both through the
+same C ABI with the per-step inputs in pinned host memory, the host->device
+copies of inputs and the device->host copies of outputs inside the timed
+region.
+
+`--impl reference` times the fp64 CPU oracle (the correctness yardstick, not
+a tuned program) on bounded samples of the same workloads.
+
+Multi-GPU (torchrun): every rank runs its own independent copy of the
+workloads (seeded by rank), no collective on the data path; timings are
+bracketed by barriers and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s and decode tokens/s on 1 GB300; % of tensor/HBM roofline"
+HBM_FALLBACK_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def _src_sha(name):
+    path = os.path.join(ROOT, "gated_delta_rule_46_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _ncu_traffic(kernel_key, src_file):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source has changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)[kernel_key]
+        if d.get("source_sha") != _src_sha(src_file):
+            return None
+        return int(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.result = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if sm:
+            self.result = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                           "reasons": sorted(reasons), "samples": len(sm)}
+        return False
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# --------------------------------------------------------------------------- CPU arms
+
+def _oracle_sample(budget_s=12.0, threads=None):
+    """The oracle on bounded samples: the full prefill workload repeated until
+    about half the budget is spent, and a slice of the decode workload."""
+    import numpy as np
+    import oracle
+    from gated_delta_rule_46_gb300 import inputs
+    threads = threads or (os.cpu_count() or 1)
+    oracle.build()
+    w1 = inputs.workload(1)
+    d = inputs.prefill_inputs(w1)
+    reps, t_pref = 0, 0.0
+    while t_pref < budget_s / 2 or reps == 0:
+        t0 = time.perf_counter()
+        oracle.prefill(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], d["cu_seqlens"],
+                       d["initial_state"], threads=threads)
+        t_pref += time.perf_counter() - t0
+        reps += 1
+    pref_tps = reps * w1.total_tokens / t_pref
+    w4 = inputs.workload(4)
+    A = inputs.decode_A(w4)
+    st = inputs.initial_state(w4).double().numpy()
+    steps, t_dec = 0, 0.0
+    while t_dec < budget_s / 2 or steps == 0:
+        dd = inputs.decode_inputs(w4, steps % w4.decode_steps)
+        t0 = time.perf_counter()
+        _, st = oracle.decode_step(dd["q"], dd["k"], dd["v"], dd["z"], A, dd["beta"], st,
+                                   threads=threads)
+        t_dec += time.perf_counter() - t0
+        steps += 1
+    dec_tps = steps * w4.decode_N / t_dec
+    sample = (f"prefill workload (1 x 4096 tokens, H=16, d=128) run in full {reps}x; "
+              f"decode workload (256 seqs, H=32, d=128) {steps} of its 128 steps; fp64 "
+              f"token-serial oracle, one thread per (sequence, head) chain")
+    return pref_tps, dec_tps, threads, sample, t_pref + t_dec, reps, steps
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    t_start = time.perf_counter()
+    pref_tps, dec_tps, cores, sample, cpu_s, reps, steps = _oracle_sample(
+        budget_s=max(4.0, 3.0 * (args.steps + args.warmup)))
+    wall = time.perf_counter() - t_start
+    line = {
+        "impl": "reference", "metric": METRIC, "value": pref_tps, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * 4096 / pref_tps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "KDA prefill B=1 H=16 T=4096 dk=dv=128 (oracle on host cores); "
+                               "decode N=256 H=32 dk=dv=128",
+                   "global_batch": 1, "seq_len": 4096, "parallelism": "none (CPU threads)"},
+        "decode": {"value": dec_tps, "unit": "tokens/s"},
+        "cpu_baseline": {"value": pref_tps, "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample, "decode_value": dec_tps},
+        "e2e": {"value": pref_tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_46_gb300 as kda
+    from gated_delta_rule_46_gb300 import inputs
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    seed = rank
+    kda.lib()
+
+    # ---- prefill workload, resident in HBM
+    w1 = inputs.workload(1)
+    d1 = inputs.prefill_inputs(w1, seed)
+    g1 = {n: (t.to(dev) if isinstance(t, torch.Tensor) else t) for n, t in d1.items()}
+    T1, H1 = w1.total_tokens, w1.H
+    out1 = torch.empty((T1, H1, 128), dtype=torch.bfloat16, device=dev)
+    fin1 = torch.empty((1, H1, 128, 128), dtype=torch.float32, device=dev)
+    ws1 = torch.zeros(kda.workspace_size(T1, 1, H1, 128, 128), dtype=torch.uint8, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MB > L2
+
+    # ---- decode workload: 128 steps of inputs pre-generated on the device
+    w4 = inputs.workload(4)
+    NS = w4.decode_steps
+    A4 = inputs.decode_A(w4, seed).to(dev)
+    state = inputs.initial_state(w4, seed).to(dev)
+    host_steps = [inputs.decode_inputs(w4, s, seed) for s in range(NS)]
+    dsteps = [{n: t.to(dev) for n, t in hs.items()} for hs in host_steps]
+    out4 = torch.empty((w4.decode_N, w4.H, 128), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def prefill():
+        kda.chunk_prefill(g1["q"], g1["k"], g1["v"], g1["z"], g1["A"], g1["beta"],
+                          g1["cu_seqlens"], g1["initial_state"], final_state=fin1, out=out1,
+                          workspace=ws1)
+
+    def decode_all():
+        for s in range(NS):
+            x = dsteps[s]
+            kda.decode_step(x["q"], x["k"], x["v"], x["z"], A4, x["beta"], state, out=out4)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        prefill()
+        decode_all()
+    barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        e_start.record(stream)
+        for i in range(K):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            ev[i][2].record(stream)
+            decode_all()
+            ev[i][3].record(stream)
+        e_end.record(stream)
+        barrier()
+    t_pref = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_dec = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    t_total = e_start.elapsed_time(e_end)
+
+    # ---- end to end through the C ABI with host buffers
+    pin = {n: t.pin_memory() for n, t in d1.items() if isinstance(t, torch.Tensor)}
+    host_out1 = torch.empty((T1, H1, 128), dtype=torch.bfloat16).pin_memory()
+    host_fin1 = torch.empty((1, H1, 128, 128), dtype=torch.float32).pin_memory()
+    pin_steps = [{n: t.pin_memory() for n, t in hs.items()} for hs in host_steps]
+    host_out4 = torch.empty((w4.decode_N, w4.H, 128), dtype=torch.bfloat16).pin_memory()
+    h2d_pref = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h_pref = host_out1.numel() * 2 + host_fin1.numel() * 4
+    h2d_dec = NS * sum(t.numel() * t.element_size() for t in pin_steps[0].values())
+    d2h_dec = NS * host_out4.numel() * 2
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier()
+    for i in range(K):
+        flush.fill_(float(i))
+        ee[i][0].record(stream)
+        for n, t in pin.items():
+            g1[n].copy_(t, non_blocking=True)
+        prefill()
+        host_out1.copy_(out1, non_blocking=True)
+        host_fin1.copy_(fin1, non_blocking=True)
+        ee[i][1].record(stream)
+        ee[i][2].record(stream)
+        for s in range(NS):
+            x = dsteps[s]
+            for n, t in pin_steps[s].items():
+                x[n].copy_(t, non_blocking=True)
+            kda.decode_step(x["q"], x["k"], x["v"], x["z"], A4, x["beta"], state, out=out4)
+            host_out4.copy_(out4, non_blocking=True)
+        ee[i][3].record(stream)
+    barrier()
+    e2e_pref = [ee[i][0].elapsed_time(ee[i][1]) for i in range(K)]
+    e2e_dec = [ee[i][2].elapsed_time(ee[i][3]) for i in range(K)]
+
+    def agg_max(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    tp = agg_max(sum(t_pref) / 1000.0)
+    td = agg_max(sum(t_dec) / 1000.0)
+    tt = agg_max(t_total / 1000.0)
+    e2p = agg_max(sum(e2e_pref) / 1000.0)
+    e2d = agg_max(sum(e2e_dec) / 1000.0)
+    ok_status = kda.check_device_status(ws1)
+
+    pref_tokens = world * K * T1
+    dec_tokens = world * K * NS * w4.decode_N
+    value = pref_tokens / tp
+    dec_value = dec_tokens / td
+
+    peak, peak_kind = _peaks()
+    alg_pref = (T1 * H1 * inputs.bytes_per_token_head(128, 128, 2)
+                + 2 * H1 * 128 * 128 * 4 + H1 * 128 * 4 + 8)
+    alg_dec = (w4.decode_N * w4.H * (2 * 128 * 128 * 4 + inputs.bytes_per_token_head(128, 128, 2))
+               + w4.H * 128 * 4)
+    per_launch_pref = (sum(t_pref) / K) / 1000.0
+    per_launch_dec = (sum(t_dec) / (K * NS)) / 1000.0
+    ach_pref = alg_pref / per_launch_pref / 1e9
+    ach_dec = alg_dec / per_launch_dec / 1e9
+    roof_dec = {"kernel": "decode_kernel<bf16,128,128>", "bound": "hbm", "achieved": ach_dec,
+                "peak": peak, "unit": "GB/s", "frac": ach_dec / peak,
+                "traffic": _ncu_traffic("decode_kernel", "kda_simt.cu"),
+                "algorithmic_bytes_per_launch": alg_dec, "peak_source": peak_kind,
+                "us_per_launch": per_launch_dec * 1e6}
+    roof_pref = {"kernel": "prefill_tc_kernel (+ schedule_kernel)", "bound": "hbm",
+                 "achieved": ach_pref, "peak": peak, "unit": "GB/s", "frac": ach_pref / peak,
+                 "traffic": _ncu_traffic("prefill_tc_kernel", "kda_prefill_tc.cu"),
+                 "algorithmic_bytes_per_launch": alg_pref, "peak_source": peak_kind,
+                 "us_per_launch": per_launch_pref * 1e6}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pt, dt, cores, sample, _, _, _ = _oracle_sample(budget_s=12.0)
+        cpu = {"value": pt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": sample, "decode_value": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": 1000.0 * tt / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "KDA prefill B=1 H=16 T=4096 dk=dv=128 bf16, fp32 init "
+                                   "state; + 128 decode steps N=256 H=32 dk=dv=128",
+                       "global_batch": world, "seq_len": T1,
+                       "parallelism": f"replicas x{world} (independent problems)",
+                       "l2": "flushed before every prefill (256 MB write); decode state 537 MB > L2"},
+            "decode": {"value": dec_value, "unit": "tokens/s", "us_per_step": per_launch_dec * 1e6,
+                       "roofline": roof_dec},
+            "roofline": roof_dec,
+            "roofline_prefill": roof_pref,
+            "prefill_us_per_call": per_launch_pref * 1e6,
+            "e2e": {"value": pref_tokens / e2p, "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d_pref + h2d_dec, "d2h_bytes_per_step": d2h_pref + d2h_dec,
+                    "decode_value": dec_tokens / e2d},
+            "gpu_launches": K * (2 + NS),
+            "clocks": clk.result,
+            "device_status": ok_status,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
