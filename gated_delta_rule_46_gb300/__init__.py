@@ -5,8 +5,8 @@ The compute path is the CUDA library built from ``csrc/`` (C ABI in
 seeded synthetic workloads.
 """
 from . import inputs  # noqa: F401
-from .kda import (KDAError, chunk_prefill, check_device_status, decode_step, gate,  # noqa: F401
-                  lib, library_path, workspace_size)
+from .kda import (KDAError, chunk_prefill, chunk_prefill_noalloc, check_device_status,  # noqa: F401
+                  decode_step, gate, lib, library_path, workspace_size)
 
 __all__ = ["inputs", "KDAError", "chunk_prefill", "check_device_status", "decode_step", "gate",
-           "lib", "library_path", "workspace_size"]
+           "lib", "library_path", "workspace_size", "chunk_prefill_noalloc"]

@@ -181,3 +181,40 @@ def decode_step(q, k, v, z, A, beta, state, out=None, stream=None):
                                _stream(stream))
     _raise(st, "kda_decode_step")
     return out
+
+
+def chunk_prefill_noalloc(q, k, v, z, A, beta, cu_seqlens, initial_state=None, final_state=None,
+                          out=None, stream=None):
+    """kda_chunk_prefill_noalloc: the same prefill without a caller workspace
+    (the library's fixed scratch is used; see include/kda.h).  ``out`` and
+    ``final_state`` must be given by callers that cannot allocate; when they
+    are None this wrapper allocates them with torch for convenience."""
+    L = lib()
+    fn = L.kda_chunk_prefill_noalloc
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    fn.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, I, I, P, P, P, P]
+    fn.restype = I
+    _check(q, "q")
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    for name, t in (("k", k), ("z", z)):
+        _check(t, name, (T, H, dk), q.dtype, dev)
+    _check(v, "v", (T, H, dv), q.dtype, dev)
+    _check(A, "A", (H, dk), torch.float32, dev)
+    _check(beta, "beta", (T, H), torch.float32, dev)
+    _check(cu_seqlens, "cu_seqlens", None, torch.int32, dev)
+    N = cu_seqlens.shape[0] - 1
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (N, H, dk, dv), torch.float32, dev)
+    if final_state is None:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(final_state, "final_state", (N, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _check(out, "out", (T, H, dv), q.dtype, dev)
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(cu_seqlens), N, T, H,
+            dk, dv, _dtype_code(q), _ptr(initial_state), _ptr(final_state), _ptr(out),
+            _stream(stream))
+    _raise(st, "kda_chunk_prefill_noalloc")
+    return out, final_state

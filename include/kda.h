@@ -114,6 +114,41 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
                                size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_prefill_noalloc -- kda_chunk_prefill for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this call: it is
+ * a library convenience, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc when they run a prefill: plugin code in
+ * a host application that owns the device memory and offers no allocator,
+ * serving loops whose device-memory budget is fixed at start-up, and code that
+ * must not take the allocator's implicit device synchronisation.  This call
+ * takes the same arguments as kda_chunk_prefill except the workspace, and
+ * allocates nothing: its scratch is a fixed device array inside the library
+ * (KDA_NOALLOC_MAX_SEQS * 4 + 256 bytes, about 64 KiB), which every GPU that
+ * loads the library holds until the process exits.
+ *   - num_seqs above KDA_NOALLOC_MAX_SEQS returns KDA_ERR_UNSUPPORTED, before
+ *     anything is launched.
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one scratch array.  Each call resets
+ *     the parts that must start at zero, but calls that overlap on the GPU
+ *     (concurrent streams, or other host threads) race on it: serialise them.
+ *   - Device-side conditions (malformed offsets, an expired wait) are recorded
+ *     in that shared scratch and are not reported by this call; use
+ *     kda_chunk_prefill with a workspace and kda_check_device_status to see
+ *     them.
+ * Results are identical to kda_chunk_prefill's for the same arguments.
+ */
+#define KDA_NOALLOC_MAX_SEQS 16384
+kda_status_t kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
+                                       const void *z, const float *A, const float *beta,
+                                       const int32_t *cu_seqlens, int num_seqs,
+                                       int64_t total_tokens, int H, int dk, int dv,
+                                       kda_dtype_t dtype, const float *initial_state,
+                                       float *final_state, void *out, kda_stream_t stream);
+
+/*
  * kda_decode_step -- one new token for each of N sequences; the recurrent
  * state is read and updated IN PLACE (the fixed-size state that replaces the
  * KV cache, "Sequence mixing").
