@@ -33,11 +33,12 @@ bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
 kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
 // The tensor-core prefill covers bf16 with dk = dv = 128 and needs 16-byte
-// aligned q/k/v/z for its TMA descriptors.
+// aligned q/k/v/z (TMA descriptors) and out (16-byte stores).
 bool use_tc(kda_dtype_t dt, int dk, int dv, const void *q, const void *k, const void *v,
-            const void *z, int64_t total) {
+            const void *z, const void *out, int64_t total) {
     return dt == KDA_BF16 && dk == 128 && dv == 128 && total > 0 && total < (int64_t(1) << 31) &&
-           aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(z, 16);
+           aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(z, 16) &&
+           aligned(out, 16);
 }
 
 }  // namespace
@@ -94,7 +95,7 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
     if (total_tokens > 0 && (!q || !k || !v || !z || !beta || !out)) return KDA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    if (use_tc(dtype, dk, dv, q, k, v, z, total_tokens)) {
+    if (use_tc(dtype, dk, dv, q, k, v, z, out, total_tokens)) {
         return from_cuda(kda::launch_prefill_tc(q, k, v, z, A, beta, cu_seqlens, num_seqs,
                                                 total_tokens, H, initial_state, final_state, out,
                                                 workspace, st));

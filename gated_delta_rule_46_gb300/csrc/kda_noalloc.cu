@@ -85,7 +85,8 @@ extern "C" kda_status_t kda_chunk_prefill_noalloc(
     if (scratch_on_current_device(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool tc = dtype == KDA_BF16 && dk == 128 && dv == 128 && total_tokens > 0 &&
-                    aligned16(q) && aligned16(k) && aligned16(v) && aligned16(z);
+                    aligned16(q) && aligned16(k) && aligned16(v) && aligned16(z) &&
+                    aligned16(out);
     if (tc) {
         // the schedule kernel zeroes the work counter and status word in the scratch
         return kda::launch_prefill_tc(q, k, v, z, A, beta, cu_seqlens, num_seqs, total_tokens,
