@@ -66,7 +66,8 @@ constexpr uint32_t OFF_QK = 0;         // [Q^; K^] 128 x 128 bf16 (32 KB)
 constexpr uint32_t OFF_V = 32768;      // v tile: 64 rows x 128 ch, two boxes
 constexpr uint32_t OFF_Z = 49152;      // z tile
 constexpr uint32_t OFF_VT = 65536;     // V^T [j][s] 128 x 64 bf16 (masked rows zeroed)
-constexpr uint32_t OFF_OST = 81920;    // output tile [t][j] bf16, 16-byte chunks XOR t % 16
+constexpr uint32_t OFF_OST = 81920;    // output tile: two 64-channel boxes in the TMA 128B-swizzle layout
+constexpr uint32_t OFF_PB = 81920;     // P [t][s]: 64 x 64 bf16 (phases B-C, before the output tile)
 constexpr uint32_t OFF_GB = 98304;     // right factors: 160 rows (tile a at row 16a(a+1)/2) x 128
 constexpr uint32_t GB_KBLK = 160 * 128;
 constexpr uint32_t OFF_B1 = 139264;    // [K~; Q~] 128 x 128 bf16 (B of the state MMA)
@@ -75,9 +76,8 @@ constexpr int LSTR = 68;               // float32 row stride of L and Y (16-byte
 constexpr uint32_t OFF_L = 98304;      // L [64][LSTR] float32
 constexpr uint32_t OFF_Y = OFF_L + 64 * LSTR * 4;      // Y = (I + L)^{-1}
 constexpr uint32_t OFF_W = OFF_Y + 64 * LSTR * 4;      // W_am = Y_aa L_am, 6 blocks of 16 x 16
-constexpr uint32_t OFF_TB = 139264;    // T [t][s]: 64 x 64 bf16
-constexpr uint32_t OFF_PB = 147456;    // P [t][s]: 64 x 64 bf16
-constexpr uint32_t OFF_RU = 155648;    // RHS^T, then U^T: 128 x 64 bf16
+constexpr uint32_t OFF_TB = 139264;    // T [t][s]: 64 x 64 bf16 (after the state MMA)
+constexpr uint32_t OFF_RU = 155648;    // RHS^T, then U^T: 128 x 64 bf16 (after the state MMA)
 constexpr uint32_t OFF_KE = 172032;    // Kend^T [c][s] 128 x 64 bf16
 constexpr uint32_t OFF_ST = 188416;    // S^T [j][c] 128 x 128 bf16 (A of the state MMA)
 constexpr uint32_t OFF_MISC = 221184;
@@ -224,7 +224,7 @@ __device__ __forceinline__ void tma_2box(uint8_t *dst, const CUtensorMap *tm, in
 __global__ void __launch_bounds__(NT, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
-                  const Params p) {
+                  const __grid_constant__ CUtensorMap tm_o, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -270,6 +270,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
         ptx::prefetch_tensormap(&tm_z);
+        ptx::prefetch_tensormap(&tm_o);
         *s_abort = 0;
     }
     if (warp == 0) {
@@ -455,6 +456,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (*s_abort) break;
             if (tid == 0) {
                 ptx::tc_fence_after_sync();
+                ptx::bulk_wait_read();   // the previous output tile has left OST (P goes there next)
                 // every thread has read its z rows: prefetch the next chunk's
                 if (has_next) tma_2box(sm + OFF_Z, &tm_z, hx, (int)next_row, bar_z);
                 // Gram/P: D[r][tile_off(a) + s] = [Q^;K^][r] . B[tile_off(a) + s], all four tiles
@@ -473,7 +475,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
             if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, hx, (int)next_row, bar_qk);
             if (has_next) ++qk_issued;
-            if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
             if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
             {
@@ -577,6 +578,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             __syncthreads();
             solve_level(3, Ym, Wm, tid);
             __syncthreads();
+            // the state MMA (still reading B1, where T and RHS go) overlapped the solve
+            if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
+            ptx::tc_fence_after_sync();
             {
                 // T = Y Diag(beta), lower triangle, bf16; 8 columns per thread
                 const int t = tid >> 3, q8 = tid & 7;
@@ -659,31 +663,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
                     st_chunk(sm + OFF_ST + (cg >> 1) * 16384, swz(ch, 4 * (cg & 1) + q4), &X[8 * q4]);
-                // O tile staged as [t][j] bf16, 16-byte chunks XOR-swizzled by t % 16
-                const int jc = ch >> 3, jin = (ch & 7) * 2;
+                // O tile staged in the TMA layout: box j/64, row t, 16-byte chunk XOR t % 8
+                const uint32_t obox = OFF_OST + (ch >> 6) * 8192;
+                const int jc = (ch & 63) >> 3, jin = (ch & 7) * 2;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int t = 16 * cg + i;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST + t * 256 + ((jc ^ (t & 15)) << 4) + jin) =
-                        __float2bfloat16_rn(O[i]);
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + obox + swz(t, jc) + jin) = __float2bfloat16_rn(O[i]);
                 }
             }
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
-            {
+            if (*s_abort) break;
+            if (nvalid == C) {
+                if (tid == 0) {
+                    ptx::tma_store_2d(&tm_o, hx, (int)row0, sm + OFF_OST);
+                    ptx::tma_store_2d(&tm_o, hx + 64, (int)row0, sm + OFF_OST + 8192);
+                    ptx::bulk_commit();
+                }
+            } else {
+                // ragged last chunk: only rows < nvalid may be written
                 const int t = tid >> 3, part = tid & 7;
                 if (t < nvalid) {
                     __nv_bfloat16 *dst = p.out + (row0 + t) * rowstride + hx;
 #pragma unroll
                     for (int k2 = 0; k2 < 2; ++k2) {
-                        const int cc = 2 * part + k2;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(sm + OFF_OST + t * 256 + ((cc ^ (t & 15)) << 4));
+                        const int cc = 2 * part + k2;     // 16-byte chunk of the 256-byte row
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            sm + OFF_OST + (cc >> 3) * 8192 + swz(t, cc & 7));
                         *reinterpret_cast<uint4 *>(dst + cc * 8) = v;
                     }
                 }
             }
-            if (*s_abort) break;
         }
         if (*s_abort) break;
         if (p.final_state) {
@@ -709,6 +721,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
         while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
     }
+    if (tid == 0) ptx::bulk_wait_all();   // output stores done before shared memory goes away
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -762,9 +775,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
                               void *out, void *workspace, cudaStream_t st) {
-    CUtensorMap mq, mk, mv, mz;
+    CUtensorMap mq, mk, mv, mz, mo;
     if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) ||
-        !make_map(&mv, v, total, H) || !make_map(&mz, z, total, H))
+        !make_map(&mv, v, total, H) || !make_map(&mz, z, total, H) ||
+        !make_map(&mo, out, total, H))
         return cudaErrorInvalidValue;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(ws + kWsStatus);
@@ -786,7 +800,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
     prm.counter = counter; prm.status = status; prm.total_tokens = total;
     prm.num_seqs = num_seqs; prm.H = H;
-    tc::prefill_tc_kernel<<<grid, tc::NT, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mz, prm);
+    tc::prefill_tc_kernel<<<grid, tc::NT, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mz, mo, prm);
     return cudaGetLastError();
 }
 
