@@ -338,7 +338,7 @@ def run_gpu(args):
                 "traffic": _ncu_traffic("decode_kernel", "kda_simt.cu"),
                 "algorithmic_bytes_per_launch": alg_dec, "peak_source": peak_kind,
                 "us_per_launch": per_launch_dec * 1e6}
-    roof_pref = {"kernel": "prefill_tc_kernel (+ schedule_kernel)", "bound": "hbm",
+    roof_pref = {"kernel": "kda_chunk_prefill (schedule + intra-chunk + state-pass kernels)", "bound": "hbm",
                  "achieved": ach_pref, "peak": peak, "unit": "GB/s", "frac": ach_pref / peak,
                  "traffic": _ncu_traffic("prefill_tc_kernel", "kda_prefill_tc.cu"),
                  "algorithmic_bytes_per_launch": alg_pref, "peak_source": peak_kind,
@@ -369,7 +369,7 @@ def run_gpu(args):
             "e2e": {"value": pref_tokens / e2p, "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d_pref + h2d_dec, "d2h_bytes_per_step": d2h_pref + d2h_dec,
                     "decode_value": dec_tokens / e2d},
-            "gpu_launches": K * (2 + NS),
+            "gpu_launches": K * (3 + NS),
             "clocks": clk.result,
             "device_status": ok_status,
             "cpu_baseline": cpu,

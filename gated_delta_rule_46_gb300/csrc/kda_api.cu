@@ -21,7 +21,8 @@ cudaError_t launch_prefill_serial(const void *q, const void *k, const void *v, c
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
-                              void *out, void *workspace, cudaStream_t st);
+                              void *out, void *workspace, size_t workspace_bytes, cudaStream_t st);
+size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H);
 }  // namespace kda
 
 namespace {
@@ -70,10 +71,16 @@ kda_status_t kda_gate(const void *z, kda_dtype_t z_dtype, const float *A, float 
 
 size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
                                   kda_dtype_t dtype) {
-    (void)total_tokens; (void)H; (void)dk; (void)dv; (void)dtype;
     if (num_seqs < 0) num_seqs = 0;
     size_t bytes = kda::kWsOrder + sizeof(int32_t) * (size_t)num_seqs;
-    return (bytes + 255) & ~size_t(255);
+    bytes = (bytes + 255) & ~size_t(255);
+    // the tensor-core path can also use room for its split (few-chain) plan
+    if (dtype == KDA_BF16 && dk == 128 && dv == 128 && H > 0 && total_tokens > 0 &&
+        total_tokens < (int64_t(1) << 31)) {
+        const size_t extra = kda::prefill_tc_workspace_bytes(total_tokens, num_seqs, H);
+        if (extra > bytes) bytes = (extra + 255) & ~size_t(255);
+    }
+    return bytes;
 }
 
 kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,
@@ -87,8 +94,9 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
     if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
     if (total_tokens >= (int64_t(1) << 31) || (int64_t)num_seqs * H >= (int64_t(1) << 31))
         return KDA_ERR_UNSUPPORTED;
-    if (!workspace || !aligned(workspace, 16) ||
-        workspace_bytes < kda_prefill_workspace_size(total_tokens, num_seqs, H, dk, dv, dtype))
+    // the schedule area is required; room for the split plan is optional
+    const size_t min_bytes = (kda::kWsOrder + sizeof(int32_t) * (size_t)num_seqs + 255) & ~size_t(255);
+    if (!workspace || !aligned(workspace, 16) || workspace_bytes < min_bytes)
         return KDA_ERR_INVALID_ARG;
     if (num_seqs == 0) return KDA_OK;
     if (!cu_seqlens || !A) return KDA_ERR_INVALID_ARG;
@@ -98,7 +106,7 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
     if (use_tc(dtype, dk, dv, q, k, v, z, out, total_tokens)) {
         return from_cuda(kda::launch_prefill_tc(q, k, v, z, A, beta, cu_seqlens, num_seqs,
                                                 total_tokens, H, initial_state, final_state, out,
-                                                workspace, st));
+                                                workspace, workspace_bytes, st));
     }
     uint32_t *status = reinterpret_cast<uint32_t *>(ws + kda::kWsStatus);
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), st);

@@ -26,7 +26,7 @@ cudaError_t launch_prefill_serial(const void *q, const void *k, const void *v, c
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
-                              void *out, void *workspace, cudaStream_t st);
+                              void *out, void *workspace, size_t workspace_bytes, cudaStream_t st);
 }  // namespace kda
 
 namespace {
@@ -90,7 +90,7 @@ extern "C" kda_status_t kda_chunk_prefill_noalloc(
     if (tc) {
         // the schedule kernel zeroes the work counter and status word in the scratch
         return kda::launch_prefill_tc(q, k, v, z, A, beta, cu_seqlens, num_seqs, total_tokens,
-                                      H, initial_state, final_state, out, scratch, st) ==
+                                      H, initial_state, final_state, out, scratch, kScratchBytes, st) ==
                        cudaSuccess
                    ? KDA_OK
                    : KDA_ERR_CUDA;

@@ -191,6 +191,422 @@ __device__ __forceinline__ void solve_level(int dist, float *Ym, const float *Wm
     }
 }
 
+// Per-thread view of the CTA: shared-memory pointers and the thread's roles.
+struct Ctx {
+    uint8_t *sm;
+    float *s_beta, *s_eAn, *s_R, *s_E, *s_rho, *s_tail, *s_gamma, *Lm, *Ym, *Wm;
+    int tid, warp, lane;
+    int qw, cg, ch;        // phases B-D: TMEM lane quarter, column group, value channel j
+    int cw, kb, chk;       // phase A: first key channel, its K-block and 16-byte chunk
+    uint32_t lane_base;    // TMEM address of this warp's lane quarter
+};
+
+__device__ __forceinline__ Ctx make_ctx(uint8_t *sm, uint32_t tmem) {
+    Ctx x;
+    x.sm = sm;
+    x.s_beta = reinterpret_cast<float *>(sm + OFF_BETA);
+    x.s_eAn = reinterpret_cast<float *>(sm + OFF_EAN);
+    x.s_R = reinterpret_cast<float *>(sm + OFF_R);
+    x.s_E = reinterpret_cast<float *>(sm + OFF_E);
+    x.s_rho = reinterpret_cast<float *>(sm + OFF_RHO);
+    x.s_tail = reinterpret_cast<float *>(sm + OFF_TAIL);
+    x.s_gamma = reinterpret_cast<float *>(sm + OFF_GAMMA);
+    x.Lm = reinterpret_cast<float *>(sm + OFF_L);
+    x.Ym = reinterpret_cast<float *>(sm + OFF_Y);
+    x.Wm = reinterpret_cast<float *>(sm + OFF_W);
+    x.tid = threadIdx.x;
+    x.warp = x.tid >> 5;
+    x.lane = x.tid & 31;
+    x.qw = x.warp & 3;
+    x.cg = x.warp >> 2;
+    x.ch = 32 * x.qw + x.lane;
+    x.cw = 8 * x.warp;
+    x.kb = x.warp >> 3;
+    x.chk = x.warp & 7;
+    x.lane_base = tmem + ((uint32_t)(32 * x.qw) << 16);
+    return x;
+}
+
+// Phase A of a chunk: bounded gate and log2-domain cumulative decay (rows lane
+// and lane + 32, 8 key channels per warp; scans over the lanes), the 16-token
+// tile references and their factors, and the operand tiles: [Q^; K^] in place
+// over the q/k tiles, the right factors of the four Gram/P tiles, [K~; Q~] and
+// Kend^T.  Waits for the z and q/k tiles itself.
+__device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, uint64_t *bar_z,
+                                                    uint32_t &z_done, uint64_t *bar_qk,
+                                                    uint32_t &qk_done, volatile int *s_abort) {
+    uint8_t *sm = x.sm;
+    const int lane = x.lane, cw = x.cw, kb = x.kb, chk = x.chk;
+    float *s_eAn = x.s_eAn;
+    float *s_R = x.s_R;
+    float *s_E = x.s_E;
+    float *s_rho = x.s_rho;
+    float *s_tail = x.s_tail;
+    float *s_gamma = x.s_gamma;
+    if (ptx::mbar_wait(bar_z, z_done & 1, kWaitBudget)) ++z_done; else *s_abort = 1;
+    float G0[8], G1[8];   // log2-domain cumulative log-decay of rows lane, lane + 32
+    {
+        float z0[8], z1[8], eAn[8];
+        const uint8_t *zt = sm + OFF_Z + kb * 8192;
+        ld_chunk(zt, swz(lane, chk), z0);
+        ld_chunk(zt, swz(lane + 32, chk), z1);
+        ld8(s_eAn + cw, eAn);
+        const bool ok0 = lane < nvalid, ok1 = lane + 32 < nvalid;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // g = g_min sigmoid(exp(A) z) = g_min / (1 + 2^(-exp(A) z log2 e))
+            float a0 = ok0 ? kGMin2 * rcp(1.f + ex2(eAn[i] * z0[i])) : 0.f;
+            float a1 = ok1 ? kGMin2 * rcp(1.f + ex2(eAn[i] * z1[i])) : 0.f;
+            // inclusive scans over the lanes: rows 0..31, then rows 32..63
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float t0 = __shfl_up_sync(0xffffffffu, a0, off);
+                const float t1 = __shfl_up_sync(0xffffffffu, a1, off);
+                if (lane >= off) { a0 += t0; a1 += t1; }
+            }
+            G0[i] = a0;
+            G1[i] = a1 + __shfl_sync(0xffffffffu, a0, 31);
+        }
+    }
+    // tile references: rows 15, 31, 47, 63 live in lanes 15 (G0), 31 (G0), 15 (G1), 31 (G1)
+    if ((lane & 15) == 15) {
+        float *d0 = s_R + (lane >> 4) * 128 + cw;          // R1 or R2
+        float *d1 = s_R + (2 + (lane >> 4)) * 128 + cw;    // R3 or G_end
+        *reinterpret_cast<float4 *>(d0) = make_float4(G0[0], G0[1], G0[2], G0[3]);
+        *reinterpret_cast<float4 *>(d0 + 4) = make_float4(G0[4], G0[5], G0[6], G0[7]);
+        *reinterpret_cast<float4 *>(d1) = make_float4(G1[0], G1[1], G1[2], G1[3]);
+        *reinterpret_cast<float4 *>(d1 + 4) = make_float4(G1[4], G1[5], G1[6], G1[7]);
+    }
+    __syncwarp();
+    if (lane < 8) {
+        const int c = cw + lane;
+        const float R1 = s_R[c], R2 = s_R[128 + c], R3 = s_R[256 + c], Ge = s_R[384 + c];
+        const float E0 = ex2(R1), E1 = ex2(R2 - R1), E2 = ex2(R3 - R2), E3 = ex2(Ge - R3);
+        s_E[c] = E0; s_E[128 + c] = E1; s_E[256 + c] = E2; s_E[384 + c] = E3;
+        s_rho[c] = 1.f; s_rho[128 + c] = ex2(R1); s_rho[256 + c] = ex2(R2);
+        s_rho[384 + c] = ex2(R3);
+        s_tail[c] = E1 * E2 * E3; s_tail[128 + c] = E2 * E3; s_tail[256 + c] = E3;
+        s_tail[384 + c] = 1.f;
+        s_gamma[c] = ex2(Ge);
+    }
+    if (ptx::mbar_wait(bar_qk, qk_done & 1, kWaitBudget)) ++qk_done; else *s_abort = 1;
+    __syncwarp();
+    {
+        const uint32_t kbo = kb * 16384;
+        const uint32_t gbk = OFF_GB + kb * GB_KBLK;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = lane + 32 * rr;
+            const int ta = r >> 4;                       // 16-token tile of this row
+            const bool ok = r < nvalid;
+            float Rb[8], rho[8], E[8], tl[8];
+            if (ta == 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) Rb[i] = 0.f;
+            } else {
+                ld8(s_R + (ta - 1) * 128 + cw, Rb);
+            }
+            ld8(s_rho + ta * 128 + cw, rho);
+            ld8(s_E + ta * 128 + cw, E);
+            ld8(s_tail + ta * 128 + cw, tl);
+            float qv[8], kv[8];
+            ld_chunk(sm + OFF_QK + kbo, swz(r, chk), qv);
+            ld_chunk(sm + OFF_QK + kbo, swz(64 + r, chk), kv);
+            float qe[8], ke[8], f[8], tk[8], tq[8], kend[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float x = (rr ? G1[i] : G0[i]) - Rb[i];   // in (-115.4, 0]
+                const float el = ok ? ex2(x) : 0.f;              // left factor
+                const float dd = ok ? ex2(-x) : 0.f;             // right factor
+                qe[i] = qv[i] * el;
+                ke[i] = kv[i] * el;
+                f[i] = kv[i] * dd;
+                tk[i] = ke[i] * rho[i];
+                tq[i] = qe[i] * rho[i];
+                kend[i] = (f[i] * E[i]) * tl[i];                 // k 2^(G_end - G_r)
+            }
+            st_chunk(sm + OFF_QK + kbo, swz(r, chk), qe);        // in place: [Q^; K^]
+            st_chunk(sm + OFF_QK + kbo, swz(64 + r, chk), ke);
+            st_chunk(sm + OFF_B1 + kbo, swz(r, chk), tk);
+            st_chunk(sm + OFF_B1 + kbo, swz(64 + r, chk), tq);
+            // Kend^T [c][s]
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = cw + i;
+                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_KE + swz(c, r >> 3) + (r & 7) * 2) =
+                    __float2bfloat16_rn(kend[i]);
+            }
+            // right factors for the Gram/P tiles a2 >= ta: k 2^(R_a2 - G_r)
+            for (int a2 = ta; a2 < 4; ++a2) {
+                st_chunk(sm + gbk, swz(tile_off(a2) + r, chk), f);
+                if (a2 < 3) {   // next tile: multiply by E_a2 = 2^(R_{a2+1} - R_a2)
+                    float en[8];
+                    if (a2 == ta) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) en[i] = E[i];
+                    } else {
+                        ld8(s_E + a2 * 128 + cw, en);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) f[i] *= en[i];
+                }
+            }
+        }
+    }
+}
+
+// P (TMEM rows 0..63 of the Gram/P accumulator) and L (rows 64..127), masked
+// to the causal pattern: P into its bf16 operand tile, L (times beta) in float32.
+__device__ __forceinline__ void phase_extract_PL(const Ctx &x, uint32_t off_pb) {
+    uint8_t *sm = x.sm;
+    const int warp = x.warp, lane = x.lane, qw = x.qw, cg = x.cg;
+    const uint32_t lane_base = x.lane_base;
+    float *s_beta = x.s_beta;
+    float *Lm = x.Lm;
+    {
+        // P (TMEM rows 0..63) and L (rows 64..127): 16 columns per thread
+        const int r = 32 * qw + lane;
+        const int t = r & 63;
+        const bool isL = r >= 64;
+        const int m = qw & 1;                 // this warp sees tiles 2m, 2m+1
+        const int a = 2 * m + (lane >> 4);
+        const int colbase = 16 * cg;
+        float X[16], Y[16];
+        const bool loadX = cg <= 2 * m, loadY = cg <= 2 * m + 1;   // warp-uniform
+        if (loadX) ptx::tmem_ld16(lane_base + TM_G + tile_off(2 * m) + colbase, X);
+        if (loadY) ptx::tmem_ld16(lane_base + TM_G + tile_off(2 * m + 1) + colbase, Y);
+        ptx::tmem_ld_wait();
+        const bool have = cg <= a;
+        const float bt = s_beta[t];
+        float vals[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int s = colbase + i;
+            const float d = have ? ((lane < 16) ? X[i] : Y[i]) : 0.f;
+            vals[i] = isL ? ((s < t) ? bt * d : 0.f) : ((s <= t) ? d : 0.f);
+        }
+        if (isL) {
+            float4 *dst = reinterpret_cast<float4 *>(Lm + t * LSTR + colbase);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_float4(vals[4 * i], vals[4 * i + 1], vals[4 * i + 2], vals[4 * i + 3]);
+        } else {
+            st_chunk(sm + off_pb, swz(t, 2 * cg), &vals[0]);
+            st_chunk(sm + off_pb, swz(t, 2 * cg + 1), &vals[8]);
+        }
+    }
+}
+
+// Warps 0-3: the four diagonal 16 x 16 blocks of (I + L)^{-1} by forward
+// substitution (one column per lane); the other warps meanwhile transpose the
+// v tile into V^T [j][s], rows past the sequence end zeroed.
+__device__ __forceinline__ void phase_diag_and_vt(const Ctx &x, int nvalid) {
+    uint8_t *sm = x.sm;
+    const int warp = x.warp, lane = x.lane;
+    float *Lm = x.Lm;
+    float *Ym = x.Ym;
+    if (warp < 4) {
+        // diagonal 16 x 16 blocks of (I + L)^{-1} by forward substitution, one column per lane
+        if (lane < 16) {
+            const int b0 = 16 * warp;
+            float y[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float lr[16];
+                const float *src = Lm + (b0 + i) * LSTR + b0;
+                ld8(src, lr); ld8(src + 8, lr + 8);
+                float a0 = (i == lane) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+                for (int mm = 0; mm < i; ++mm) {
+                    if (mm & 1) a1 -= lr[mm] * y[mm]; else a0 -= lr[mm] * y[mm];
+                }
+                y[i] = a0 + a1;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Ym[(b0 + i) * LSTR + b0 + lane] = y[i];
+        }
+    } else {
+        // meanwhile: V^T [j][s] (rows past the sequence end zeroed); a warp
+        // transposes one 8-channel chunk, lane = rows lane and lane + 32
+        for (int cc = warp - 4; cc < 16; cc += 12) {
+            float v0[8], v1[8];
+            const uint8_t *vt = sm + OFF_V + (cc >> 3) * 8192;
+            ld_chunk(vt, swz(lane, cc & 7), v0);
+            ld_chunk(vt, swz(lane + 32, cc & 7), v1);
+            const bool ok0 = lane < nvalid, ok1 = lane + 32 < nvalid;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = 8 * cc + i;
+                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, lane >> 3) + (lane & 7) * 2) =
+                    __float2bfloat16_rn(ok0 ? v0[i] : 0.f);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, 4 + (lane >> 3)) + (lane & 7) * 2) =
+                    __float2bfloat16_rn(ok1 ? v1[i] : 0.f);
+            }
+        }
+    }
+}
+
+// W_am = Y_aa L_am for the six blocks below the diagonal (1 x 4 outputs per task).
+__device__ __forceinline__ void phase_W(const Ctx &x) {
+    const int tid = x.tid;
+    float *Lm = x.Lm;
+    float *Ym = x.Ym;
+    float *Wm = x.Wm;
+    // W_am = Y_aa L_am for the six blocks below the diagonal (1 x 4 outputs per task)
+    for (int task = tid; task < 6 * 64; task += NT) {
+        const int blk = task >> 6, i = (task >> 2) & 15, jj = task & 3;
+        const int a = blk < 1 ? 1 : (blk < 3 ? 2 : 3);
+        const int m = blk - (a * (a - 1)) / 2;
+        float yr[16];
+        const float *src = Ym + (16 * a + i) * LSTR + 16 * a;
+        ld8(src, yr); ld8(src + 8, yr + 8);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            float lv[4];
+            ld4(Lm + (16 * a + n) * LSTR + 16 * m + 4 * jj, lv);
+            acc[0] += yr[n] * lv[0]; acc[1] += yr[n] * lv[1];
+            acc[2] += yr[n] * lv[2]; acc[3] += yr[n] * lv[3];
+        }
+        *reinterpret_cast<float4 *>(Wm + blk * 256 + i * 16 + 4 * jj) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+}
+
+// T = Y Diag(beta), lower triangle, into its bf16 operand tile; 8 columns per thread.
+__device__ __forceinline__ void phase_T(const Ctx &x, uint32_t off_tb) {
+    uint8_t *sm = x.sm;
+    const int tid = x.tid;
+    float *s_beta = x.s_beta;
+    float *Ym = x.Ym;
+    {
+        // T = Y Diag(beta), lower triangle, bf16; 8 columns per thread
+        const int t = tid >> 3, q8 = tid & 7;
+        float tv[8], yr[8], bv[8];
+        ld8(Ym + t * LSTR + 8 * q8, yr);
+        ld8(s_beta + 8 * q8, bv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tv[i] = (8 * q8 + i <= t) ? yr[i] * bv[i] : 0.f;
+        st_chunk(sm + off_tb, swz(t, q8), tv);
+    }
+}
+
+// ---- state-pass pieces shared by the fused and the state-only kernels ------
+
+// Start state: float32 master S^T[j][c] into TMEM (the dS accumulator) and its
+// bf16 copy into the state operand tile; src == nullptr means zeros.  This
+// thread holds c in [32 cg, 32 cg + 32) of row j.
+__device__ __forceinline__ void load_state(const Ctx &x, const float *src, uint32_t tm_s,
+                                           uint32_t off_st) {
+    float Sm[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) Sm[i] = src ? src[(int64_t)(32 * x.cg + i) * D + x.ch] : 0.f;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+        st_chunk(x.sm + off_st + (x.cg >> 1) * 16384, swz(x.ch, 4 * (x.cg & 1) + q4), &Sm[8 * q4]);
+    ptx::tmem_st32(x.lane_base + tm_s + 32 * x.cg, Sm);
+    ptx::tmem_st_wait();
+}
+
+// Master state out of TMEM into dst [dk][dv] (row c, column j).
+__device__ __forceinline__ void save_state(const Ctx &x, float *dst, uint32_t tm_s) {
+    float X[32];
+    ptx::tmem_ld32(x.lane_base + tm_s + 32 * x.cg, X);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * x.cg + i) * D + x.ch] = X[i];
+}
+
+// RHS^T[j][s] = V^T[j][s] - (K~ S0)^T[j][s], 16 columns per thread.
+__device__ __forceinline__ void phase_rhs(const Ctx &x, uint32_t tm_ks, uint32_t off_vt,
+                                          uint32_t off_ru) {
+    float KS[16], vt[16];
+    ptx::tmem_ld16(x.lane_base + tm_ks + 16 * x.cg, KS);
+    ld_chunk(x.sm + off_vt, swz(x.ch, 2 * x.cg), vt);
+    ld_chunk(x.sm + off_vt, swz(x.ch, 2 * x.cg + 1), vt + 8);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) vt[i] -= KS[i];
+    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg), vt);
+    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg + 1), vt + 8);
+}
+
+// U^T into its bf16 operand tile, and S^T <- S^T Diag(2^G_end) in TMEM (the
+// dS MMA then accumulates onto it).
+__device__ __forceinline__ void phase_u_scale(const Ctx &x, uint32_t tm_u, uint32_t tm_s,
+                                              uint32_t off_ru, const float *gamma) {
+    float U[16], Sx[32], gm[32];
+    ptx::tmem_ld16(x.lane_base + tm_u + 16 * x.cg, U);
+    ptx::tmem_ld32(x.lane_base + tm_s + 32 * x.cg, Sx);
+    const float *g = gamma + 32 * x.cg;
+    ld8(g, gm); ld8(g + 8, gm + 8); ld8(g + 16, gm + 16); ld8(g + 24, gm + 24);
+    ptx::tmem_ld_wait();
+    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg), U);
+    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg + 1), U + 8);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) Sx[i] *= gm[i];
+    ptx::tmem_st32(x.lane_base + tm_s + 32 * x.cg, Sx);
+    ptx::tmem_st_wait();
+}
+
+// New state's bf16 copy into the state operand tile; O^T out of TMEM into the
+// output staging tile (two 64-channel boxes in the TMA 128B-swizzle layout).
+__device__ __forceinline__ void phase_state_out(const Ctx &x, uint32_t tm_s, uint32_t tm_o,
+                                                uint32_t off_st, uint32_t off_ost) {
+    float X[32], O[16];
+    ptx::tmem_ld32(x.lane_base + tm_s + 32 * x.cg, X);
+    ptx::tmem_ld16(x.lane_base + tm_o + 16 * x.cg, O);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+        st_chunk(x.sm + off_st + (x.cg >> 1) * 16384, swz(x.ch, 4 * (x.cg & 1) + q4), &X[8 * q4]);
+    const uint32_t obox = off_ost + (x.ch >> 6) * 8192;
+    const int jc = (x.ch & 63) >> 3, jin = (x.ch & 7) * 2;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int t = 16 * x.cg + i;
+        *reinterpret_cast<__nv_bfloat16 *>(x.sm + obox + swz(t, jc) + jin) = __float2bfloat16_rn(O[i]);
+    }
+}
+
+// The staged output tile to global memory (after a block barrier): one TMA
+// tile store per 64-channel box for a full chunk, plain 16-byte stores of the
+// rows < nvalid for the ragged last chunk of a sequence.
+__device__ __forceinline__ void store_output(const Ctx &x, const CUtensorMap *tm_o, uint32_t off_ost,
+                                             __nv_bfloat16 *out, int64_t row0, int nvalid, int hx,
+                                             int64_t rowstride) {
+    if (nvalid == C) {
+        if (x.tid == 0) {
+            ptx::tma_store_2d(tm_o, hx, (int)row0, x.sm + off_ost);
+            ptx::tma_store_2d(tm_o, hx + 64, (int)row0, x.sm + off_ost + 8192);
+            ptx::bulk_commit();
+        }
+    } else {
+        const int t = x.tid >> 3, part = x.tid & 7;
+        if (t < nvalid) {
+            __nv_bfloat16 *dst = out + (row0 + t) * rowstride + hx;
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int cc = 2 * part + k2;     // 16-byte chunk of the 256-byte row
+                const uint4 v = *reinterpret_cast<const uint4 *>(x.sm + off_ost + (cc >> 3) * 8192 + swz(t, cc & 7));
+                *reinterpret_cast<uint4 *>(dst + cc * 8) = v;
+            }
+        }
+    }
+}
+
+// Sequence bounds with the kernel's own bounds check: malformed offsets are
+// reported and the sequence treated as empty.
+__device__ __forceinline__ void seq_bounds(const int32_t *cu, int seq, int64_t total, uint32_t *status,
+                                           int tid, int64_t &bos, int64_t &eos) {
+    bos = cu[seq];
+    eos = cu[seq + 1];
+    if (bos < 0 || eos < bos || eos > total) {
+        if (tid == 0) report_status(status, kDevBadSeqlens);
+        bos = eos = 0;
+    }
+}
+
 struct Params {
     const float *A;            // [H, 128]
     const float *beta;         // [T, H]
@@ -221,6 +637,21 @@ __device__ __forceinline__ void tma_2box(uint8_t *dst, const CUtensorMap *tm, in
     ptx::tma_load_2d(dst + 8192, tm, hx + 64, y, bar);
 }
 
+// The blocked inverse after the diagonal blocks: W, then three levels.
+__device__ __forceinline__ void solve_offdiag(const Ctx &x) {
+    phase_W(x);
+    __syncthreads();
+    solve_level(1, x.Ym, x.Wm, x.tid);
+    __syncthreads();
+    solve_level(2, x.Ym, x.Wm, x.tid);
+    __syncthreads();
+    solve_level(3, x.Ym, x.Wm, x.tid);
+    __syncthreads();
+}
+
+// Fused kernel: one CTA per SM, persistent over (sequence, head) chains taken
+// longest-first; every chunk runs phases A-D above.  Used when the batch has
+// enough chains to fill the GPU.
 __global__ void __launch_bounds__(NT, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -229,13 +660,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(sm);
-    float *s_beta = reinterpret_cast<float *>(sm + OFF_BETA);
-    float *s_eAn = reinterpret_cast<float *>(sm + OFF_EAN);
-    float *s_R = reinterpret_cast<float *>(sm + OFF_R);
-    float *s_E = reinterpret_cast<float *>(sm + OFF_E);
-    float *s_rho = reinterpret_cast<float *>(sm + OFF_RHO);
-    float *s_tail = reinterpret_cast<float *>(sm + OFF_TAIL);
-    float *s_gamma = reinterpret_cast<float *>(sm + OFF_GAMMA);
     uint64_t *bar_qk = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *bar_z = bar_qk + 1;
     uint64_t *bar_v = bar_qk + 2;
@@ -245,21 +669,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + OFF_SLOT);
     volatile int *s_work = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 4);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 8);
-    float *Lm = reinterpret_cast<float *>(sm + OFF_L);
-    float *Ym = reinterpret_cast<float *>(sm + OFF_Y);
-    float *Wm = reinterpret_cast<float *>(sm + OFF_W);
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    // phases B-D: value channel j == TMEM lane, 16/32-column group cg
-    const int qw = warp & 3;           // TMEM lane quarter this warp may access
-    const int cg = warp >> 2;          // 0..3
-    const int ch = 32 * qw + lane;
-    // phase A: 8 key channels per warp, rows lane and lane + 32 per lane (rows
-    // 8 apart land on distinct swizzled bank groups)
-    const int cw = 8 * warp;
-    const int kb = warp >> 3;          // K-block (64 channels) of these channels
-    const int chk = warp & 7;          // their 16-byte chunk inside the 128-byte row
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int H = p.H;
     const int64_t rowstride = (int64_t)H * D;
 
@@ -281,7 +691,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * qw) << 16);
+    const Ctx x = make_ctx(sm, tmem);
 
     // issue / completion counters of the barriers (uniform across threads);
     // a barrier's next expected phase parity is (done & 1)
@@ -296,11 +706,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (w >= n_work || *s_abort) break;
         const int seq = p.order[w / H];
         const int h = w % H;
-        int64_t bos = p.cu_seqlens[seq], eos = p.cu_seqlens[seq + 1];
-        if (bos < 0 || eos < bos || eos > p.total_tokens) {
-            if (tid == 0) report_status(p.status, kDevBadSeqlens);
-            bos = eos = 0;
-        }
+        int64_t bos, eos;
+        seq_bounds(p.cu_seqlens, seq, p.total_tokens, p.status, tid, bos, eos);
         const int nchunks = (int)((eos - bos + C - 1) / C);
         const int64_t sidx = ((int64_t)seq * H + h) * D * D;
         const int hx = h * D;   // column of this head in the [T, H*D] view
@@ -311,23 +718,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_2box(sm + OFF_V, &tm_v, hx, (int)bos, bar_v);
         }
         if (nchunks > 0) { ++qk_issued; ++z_issued; ++v_issued; }
-
-        // ---- start state: float32 master S^T[j][c] lives in TMEM (the dS accumulator),
-        // its bf16 copy in smem; this thread holds c in [32 cg, 32 cg + 32) of row j
-        {
-            float Sm[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = 32 * cg + i;
-                Sm[i] = p.initial_state ? p.initial_state[sidx + (int64_t)c * D + ch] : 0.f;
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                st_chunk(sm + OFF_ST + (cg >> 1) * 16384, swz(ch, 4 * (cg & 1) + q4), &Sm[8 * q4]);
-            ptx::tmem_st32(lane_base + TM_D3 + 32 * cg, Sm);
-            ptx::tmem_st_wait();
-        }
-        if (tid < D) s_eAn[tid] = -expf(p.A[h * D + tid]) * kLog2e;
+        load_state(x, p.initial_state ? p.initial_state + sidx : nullptr, TM_D3, OFF_ST);
+        if (tid < D) x.s_eAn[tid] = -expf(p.A[h * D + tid]) * kLog2e;
         float beta_next = 0.f;
         if (tid < C && nchunks > 0) beta_next = (bos + tid < eos) ? p.beta[(bos + tid) * H + h] : 0.f;
         __syncthreads();   // s_eAn visible
@@ -339,117 +731,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int64_t next_row = row0 + C;
 
             // =============================== phase A: gate, cumulative decay, operands
-            if (tid < C) s_beta[tid] = beta_next;
-            if (ptx::mbar_wait(bar_z, z_done & 1, kWaitBudget)) ++z_done; else *s_abort = 1;
-            float G0[8], G1[8];   // log2-domain cumulative log-decay of rows lane, lane + 32
-            {
-                float z0[8], z1[8], eAn[8];
-                const uint8_t *zt = sm + OFF_Z + kb * 8192;
-                ld_chunk(zt, swz(lane, chk), z0);
-                ld_chunk(zt, swz(lane + 32, chk), z1);
-                ld8(s_eAn + cw, eAn);
-                const bool ok0 = lane < nvalid, ok1 = lane + 32 < nvalid;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // g = g_min sigmoid(exp(A) z) = g_min / (1 + 2^(-exp(A) z log2 e))
-                    float a0 = ok0 ? kGMin2 * rcp(1.f + ex2(eAn[i] * z0[i])) : 0.f;
-                    float a1 = ok1 ? kGMin2 * rcp(1.f + ex2(eAn[i] * z1[i])) : 0.f;
-                    // inclusive scans over the lanes: rows 0..31, then rows 32..63
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float t0 = __shfl_up_sync(0xffffffffu, a0, off);
-                        const float t1 = __shfl_up_sync(0xffffffffu, a1, off);
-                        if (lane >= off) { a0 += t0; a1 += t1; }
-                    }
-                    G0[i] = a0;
-                    G1[i] = a1 + __shfl_sync(0xffffffffu, a0, 31);
-                }
-            }
-            // tile references: rows 15, 31, 47, 63 live in lanes 15 (G0), 31 (G0), 15 (G1), 31 (G1)
-            if ((lane & 15) == 15) {
-                float *d0 = s_R + (lane >> 4) * 128 + cw;          // R1 or R2
-                float *d1 = s_R + (2 + (lane >> 4)) * 128 + cw;    // R3 or G_end
-                *reinterpret_cast<float4 *>(d0) = make_float4(G0[0], G0[1], G0[2], G0[3]);
-                *reinterpret_cast<float4 *>(d0 + 4) = make_float4(G0[4], G0[5], G0[6], G0[7]);
-                *reinterpret_cast<float4 *>(d1) = make_float4(G1[0], G1[1], G1[2], G1[3]);
-                *reinterpret_cast<float4 *>(d1 + 4) = make_float4(G1[4], G1[5], G1[6], G1[7]);
-            }
-            __syncwarp();
-            if (lane < 8) {
-                const int c = cw + lane;
-                const float R1 = s_R[c], R2 = s_R[128 + c], R3 = s_R[256 + c], Ge = s_R[384 + c];
-                const float E0 = ex2(R1), E1 = ex2(R2 - R1), E2 = ex2(R3 - R2), E3 = ex2(Ge - R3);
-                s_E[c] = E0; s_E[128 + c] = E1; s_E[256 + c] = E2; s_E[384 + c] = E3;
-                s_rho[c] = 1.f; s_rho[128 + c] = ex2(R1); s_rho[256 + c] = ex2(R2);
-                s_rho[384 + c] = ex2(R3);
-                s_tail[c] = E1 * E2 * E3; s_tail[128 + c] = E2 * E3; s_tail[256 + c] = E3;
-                s_tail[384 + c] = 1.f;
-                s_gamma[c] = ex2(Ge);
-            }
-            if (ptx::mbar_wait(bar_qk, qk_done & 1, kWaitBudget)) ++qk_done; else *s_abort = 1;
-            __syncwarp();
-            {
-                const uint32_t kbo = kb * 16384;
-                const uint32_t gbk = OFF_GB + kb * GB_KBLK;
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int r = lane + 32 * rr;
-                    const int ta = r >> 4;                       // 16-token tile of this row
-                    const bool ok = r < nvalid;
-                    float Rb[8], rho[8], E[8], tl[8];
-                    if (ta == 0) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) Rb[i] = 0.f;
-                    } else {
-                        ld8(s_R + (ta - 1) * 128 + cw, Rb);
-                    }
-                    ld8(s_rho + ta * 128 + cw, rho);
-                    ld8(s_E + ta * 128 + cw, E);
-                    ld8(s_tail + ta * 128 + cw, tl);
-                    float qv[8], kv[8];
-                    ld_chunk(sm + OFF_QK + kbo, swz(r, chk), qv);
-                    ld_chunk(sm + OFF_QK + kbo, swz(64 + r, chk), kv);
-                    float qe[8], ke[8], f[8], tk[8], tq[8], kend[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float x = (rr ? G1[i] : G0[i]) - Rb[i];   // in (-115.4, 0]
-                        const float el = ok ? ex2(x) : 0.f;              // left factor
-                        const float dd = ok ? ex2(-x) : 0.f;             // right factor
-                        qe[i] = qv[i] * el;
-                        ke[i] = kv[i] * el;
-                        f[i] = kv[i] * dd;
-                        tk[i] = ke[i] * rho[i];
-                        tq[i] = qe[i] * rho[i];
-                        kend[i] = (f[i] * E[i]) * tl[i];                 // k 2^(G_end - G_r)
-                    }
-                    st_chunk(sm + OFF_QK + kbo, swz(r, chk), qe);        // in place: [Q^; K^]
-                    st_chunk(sm + OFF_QK + kbo, swz(64 + r, chk), ke);
-                    st_chunk(sm + OFF_B1 + kbo, swz(r, chk), tk);
-                    st_chunk(sm + OFF_B1 + kbo, swz(64 + r, chk), tq);
-                    // Kend^T [c][s]
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int c = cw + i;
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_KE + swz(c, r >> 3) + (r & 7) * 2) =
-                            __float2bfloat16_rn(kend[i]);
-                    }
-                    // right factors for the Gram/P tiles a2 >= ta: k 2^(R_a2 - G_r)
-                    for (int a2 = ta; a2 < 4; ++a2) {
-                        st_chunk(sm + gbk, swz(tile_off(a2) + r, chk), f);
-                        if (a2 < 3) {   // next tile: multiply by E_a2 = 2^(R_{a2+1} - R_a2)
-                            float en[8];
-                            if (a2 == ta) {
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) en[i] = E[i];
-                            } else {
-                                ld8(s_E + a2 * 128 + cw, en);
-                            }
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) f[i] *= en[i];
-                        }
-                    }
-                }
-            }
+            if (tid < C) x.s_beta[tid] = beta_next;
+            phase_gate_operands(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -477,132 +760,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (has_next) ++qk_issued;
             if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            {
-                // P (TMEM rows 0..63) and L (rows 64..127): 16 columns per thread
-                const int r = 32 * qw + lane;
-                const int t = r & 63;
-                const bool isL = r >= 64;
-                const int m = qw & 1;                 // this warp sees tiles 2m, 2m+1
-                const int a = 2 * m + (lane >> 4);
-                const int colbase = 16 * cg;
-                float X[16], Y[16];
-                const bool loadX = cg <= 2 * m, loadY = cg <= 2 * m + 1;   // warp-uniform
-                if (loadX) ptx::tmem_ld16(lane_base + TM_G + tile_off(2 * m) + colbase, X);
-                if (loadY) ptx::tmem_ld16(lane_base + TM_G + tile_off(2 * m + 1) + colbase, Y);
-                ptx::tmem_ld_wait();
-                const bool have = cg <= a;
-                const float bt = s_beta[t];
-                float vals[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int s = colbase + i;
-                    const float d = have ? ((lane < 16) ? X[i] : Y[i]) : 0.f;
-                    vals[i] = isL ? ((s < t) ? bt * d : 0.f) : ((s <= t) ? d : 0.f);
-                }
-                if (isL) {
-                    float4 *dst = reinterpret_cast<float4 *>(Lm + t * LSTR + colbase);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_float4(vals[4 * i], vals[4 * i + 1], vals[4 * i + 2], vals[4 * i + 3]);
-                } else {
-                    st_chunk(sm + OFF_PB, swz(t, 2 * cg), &vals[0]);
-                    st_chunk(sm + OFF_PB, swz(t, 2 * cg + 1), &vals[8]);
-                }
-            }
+            phase_extract_PL(x, OFF_PB);
             __syncthreads();
-            if (warp < 4) {
-                // diagonal 16 x 16 blocks of (I + L)^{-1} by forward substitution, one column per lane
-                if (lane < 16) {
-                    const int b0 = 16 * warp;
-                    float y[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float lr[16];
-                        const float *src = Lm + (b0 + i) * LSTR + b0;
-                        ld8(src, lr); ld8(src + 8, lr + 8);
-                        float a0 = (i == lane) ? 1.f : 0.f, a1 = 0.f;
-#pragma unroll
-                        for (int mm = 0; mm < i; ++mm) {
-                            if (mm & 1) a1 -= lr[mm] * y[mm]; else a0 -= lr[mm] * y[mm];
-                        }
-                        y[i] = a0 + a1;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) Ym[(b0 + i) * LSTR + b0 + lane] = y[i];
-                }
-            } else {
-                // meanwhile: V^T [j][s] (rows past the sequence end zeroed); a warp
-                // transposes one 8-channel chunk, lane = rows lane and lane + 32
-                for (int cc = warp - 4; cc < 16; cc += 12) {
-                    float v0[8], v1[8];
-                    const uint8_t *vt = sm + OFF_V + (cc >> 3) * 8192;
-                    ld_chunk(vt, swz(lane, cc & 7), v0);
-                    ld_chunk(vt, swz(lane + 32, cc & 7), v1);
-                    const bool ok0 = lane < nvalid, ok1 = lane + 32 < nvalid;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int j = 8 * cc + i;
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, lane >> 3) + (lane & 7) * 2) =
-                            __float2bfloat16_rn(ok0 ? v0[i] : 0.f);
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, 4 + (lane >> 3)) + (lane & 7) * 2) =
-                            __float2bfloat16_rn(ok1 ? v1[i] : 0.f);
-                    }
-                }
-            }
+            phase_diag_and_vt(x, nvalid);
             __syncthreads();
             if (tid == 0 && has_next) tma_2box(sm + OFF_V, &tm_v, hx, (int)next_row, bar_v);
             if (has_next) ++v_issued;
-            // W_am = Y_aa L_am for the six blocks below the diagonal (1 x 4 outputs per task)
-            for (int task = tid; task < 6 * 64; task += NT) {
-                const int blk = task >> 6, i = (task >> 2) & 15, jj = task & 3;
-                const int a = blk < 1 ? 1 : (blk < 3 ? 2 : 3);
-                const int m = blk - (a * (a - 1)) / 2;
-                float yr[16];
-                const float *src = Ym + (16 * a + i) * LSTR + 16 * a;
-                ld8(src, yr); ld8(src + 8, yr + 8);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    float lv[4];
-                    ld4(Lm + (16 * a + n) * LSTR + 16 * m + 4 * jj, lv);
-                    acc[0] += yr[n] * lv[0]; acc[1] += yr[n] * lv[1];
-                    acc[2] += yr[n] * lv[2]; acc[3] += yr[n] * lv[3];
-                }
-                *reinterpret_cast<float4 *>(Wm + blk * 256 + i * 16 + 4 * jj) =
-                    make_float4(acc[0], acc[1], acc[2], acc[3]);
-            }
-            __syncthreads();
-            solve_level(1, Ym, Wm, tid);
-            __syncthreads();
-            solve_level(2, Ym, Wm, tid);
-            __syncthreads();
-            solve_level(3, Ym, Wm, tid);
-            __syncthreads();
+            solve_offdiag(x);
             // the state MMA (still reading B1, where T and RHS go) overlapped the solve
             if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            {
-                // T = Y Diag(beta), lower triangle, bf16; 8 columns per thread
-                const int t = tid >> 3, q8 = tid & 7;
-                float tv[8], yr[8], bv[8];
-                ld8(Ym + t * LSTR + 8 * q8, yr);
-                ld8(s_beta + 8 * q8, bv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) tv[i] = (8 * q8 + i <= t) ? yr[i] * bv[i] : 0.f;
-                st_chunk(sm + OFF_TB, swz(t, q8), tv);
-            }
-            {
-                // RHS^T[j][s] = V^T[j][s] - (K~ S0)^T[j][s], 16 columns per thread
-                float KS[16], vt[16];
-                ptx::tmem_ld16(lane_base + TM_D1 + 16 * cg, KS);
-                ld_chunk(sm + OFF_VT, swz(ch, 2 * cg), vt);
-                ld_chunk(sm + OFF_VT, swz(ch, 2 * cg + 1), vt + 8);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) vt[i] -= KS[i];
-                st_chunk(sm + OFF_RU, swz(ch, 2 * cg), vt);
-                st_chunk(sm + OFF_RU, swz(ch, 2 * cg + 1), vt + 8);
-            }
+            phase_T(x, OFF_TB);
+            phase_rhs(x, TM_D1, OFF_VT, OFF_RU);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -621,21 +790,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // =============================== phase C: U^T to smem, output and state MMAs
             if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            {
-                float U[16], Sx[32], gm[32];
-                ptx::tmem_ld16(lane_base + TM_D2 + 16 * cg, U);
-                ptx::tmem_ld32(lane_base + TM_D3 + 32 * cg, Sx);
-                ld8(s_gamma + 32 * cg, gm); ld8(s_gamma + 32 * cg + 8, gm + 8);
-                ld8(s_gamma + 32 * cg + 16, gm + 16); ld8(s_gamma + 32 * cg + 24, gm + 24);
-                ptx::tmem_ld_wait();
-                st_chunk(sm + OFF_RU, swz(ch, 2 * cg), U);
-                st_chunk(sm + OFF_RU, swz(ch, 2 * cg + 1), U + 8);
-                // S^T <- S^T Diag(2^G_end); the dS MMA then accumulates onto it
-#pragma unroll
-                for (int i = 0; i < 32; ++i) Sx[i] *= gm[i];
-                ptx::tmem_st32(lane_base + TM_D3 + 32 * cg, Sx);
-                ptx::tmem_st_wait();
-            }
+            phase_u_scale(x, TM_D2, TM_D3, OFF_RU, x.s_gamma);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -655,56 +810,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // =============================== phase D: state update, output
             if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            {
-                float X[32], O[16];
-                ptx::tmem_ld32(lane_base + TM_D3 + 32 * cg, X);
-                ptx::tmem_ld16(lane_base + TM_D1 + 64 + 16 * cg, O);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    st_chunk(sm + OFF_ST + (cg >> 1) * 16384, swz(ch, 4 * (cg & 1) + q4), &X[8 * q4]);
-                // O tile staged in the TMA layout: box j/64, row t, 16-byte chunk XOR t % 8
-                const uint32_t obox = OFF_OST + (ch >> 6) * 8192;
-                const int jc = (ch & 63) >> 3, jin = (ch & 7) * 2;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = 16 * cg + i;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + obox + swz(t, jc) + jin) = __float2bfloat16_rn(O[i]);
-                }
-            }
+            phase_state_out(x, TM_D3, TM_D1 + 64, OFF_ST, OFF_OST);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
             if (*s_abort) break;
-            if (nvalid == C) {
-                if (tid == 0) {
-                    ptx::tma_store_2d(&tm_o, hx, (int)row0, sm + OFF_OST);
-                    ptx::tma_store_2d(&tm_o, hx + 64, (int)row0, sm + OFF_OST + 8192);
-                    ptx::bulk_commit();
-                }
-            } else {
-                // ragged last chunk: only rows < nvalid may be written
-                const int t = tid >> 3, part = tid & 7;
-                if (t < nvalid) {
-                    __nv_bfloat16 *dst = p.out + (row0 + t) * rowstride + hx;
-#pragma unroll
-                    for (int k2 = 0; k2 < 2; ++k2) {
-                        const int cc = 2 * part + k2;     // 16-byte chunk of the 256-byte row
-                        const uint4 v = *reinterpret_cast<const uint4 *>(
-                            sm + OFF_OST + (cc >> 3) * 8192 + swz(t, cc & 7));
-                        *reinterpret_cast<uint4 *>(dst + cc * 8) = v;
-                    }
-                }
-            }
+            store_output(x, &tm_o, OFF_OST, p.out, row0, nvalid, hx, rowstride);
         }
         if (*s_abort) break;
-        if (p.final_state) {
-            float X[32];
-            ptx::tmem_ld32(lane_base + TM_D3 + 32 * cg, X);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) p.final_state[sidx + (int64_t)(32 * cg + i) * D + ch] = X[i];
-        }
+        if (p.final_state) save_state(x, p.final_state + sidx, TM_D3);
         ptx::tc_fence_before_sync();
         __syncthreads();
     }
@@ -730,10 +844,367 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
+// ---- split path for batches with few chains ---------------------------------
+// With fewer (sequence, head) chains than about half the SMs, most of the GPU
+// would idle while each chain walks its chunks.  The state-independent work of
+// every chunk (gate, operands, Gram/P, the inverse) is then done first by
+// prefill_intra_kernel, over all chunks of a window in parallel, and exported
+// as one record per chunk; prefill_state_kernel (one CTA per chain) streams the
+// records with bulk copies and runs only the state-dependent MMAs.
+
+// Exported record of one chunk (bf16 operand tiles in their smem layout).
+constexpr uint32_t REC_B1 = 0;         // [K~; Q~] 128 x 128
+constexpr uint32_t REC_KE = 32768;     // Kend^T [c][s] 128 x 64
+constexpr uint32_t REC_TB = 49152;     // T [t][s] 64 x 64
+constexpr uint32_t REC_PB = 57344;     // P [t][s] 64 x 64
+constexpr uint32_t REC_VT = 65536;     // V^T [j][s] 128 x 64 (rows past the end zeroed)
+constexpr uint32_t REC_G = 81920;      // 2^(G_end), 128 float
+constexpr uint32_t REC_BYTES = 82432;
+constexpr uint32_t OFF_TB_INTRA = OFF_ST;   // the intra kernel keeps T where the state tile would be
+
+struct SplitParams {
+    const float *A;
+    const float *beta;
+    const int32_t *cu_seqlens;
+    const float *initial_state;
+    float *final_state;
+    __nv_bfloat16 *out;
+    uint8_t *records;          // [chains][W] records of this window
+    float *states;             // [chains][128][128] state carried between windows
+    uint32_t *status;
+    int64_t total_tokens;
+    int num_seqs;
+    int H;
+    int w0;                    // first chunk index of the window
+    int wn;                    // chunks in the window
+    int W;                     // record slots per chain
+};
+
+__device__ __forceinline__ void bulk_store(uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(ptx::smem_addr(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            ptx::smem_addr(sdst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar))
+        : "memory");
+}
+
+struct ItemInfo {
+    int chain, h, c;
+    int64_t row0;
+    int nvalid;
+};
+
+// Work item `it` of a window: chain it / wn, chunk w0 + it % wn; false when
+// that chunk lies past the end of its sequence.
+__device__ __forceinline__ bool item_info(const SplitParams &p, int it, ItemInfo &r) {
+    const int chain = it / p.wn;
+    const int c = p.w0 + it % p.wn;
+    const int seq = chain / p.H;
+    int64_t bos = p.cu_seqlens[seq], eos = p.cu_seqlens[seq + 1];
+    if (bos < 0 || eos < bos || eos > p.total_tokens) return false;
+    const int64_t row0 = bos + (int64_t)c * C;
+    if (row0 >= eos) return false;
+    r.chain = chain;
+    r.h = chain % p.H;
+    r.c = c;
+    r.row0 = row0;
+    r.nvalid = (int)((eos - row0) < C ? (eos - row0) : C);
+    return true;
+}
+
+__global__ void __launch_bounds__(NT, 1)
+prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
+                     const SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(sm);
+    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    uint64_t *bar_z = bar_qk + 1;
+    uint64_t *bar_v = bar_qk + 2;
+    uint64_t *bar_g = bar_qk + 3;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + OFF_SLOT);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 8);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int H = p.H;
+
+    // bad sequence offsets are reported once, by the first CTA
+    if (blockIdx.x == 0 && tid < p.num_seqs) {
+        const int64_t b = p.cu_seqlens[tid], e = p.cu_seqlens[tid + 1];
+        if (b < 0 || e < b || e > p.total_tokens) report_status(p.status, kDevBadSeqlens);
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(bar_qk + i, 1);
+        ptx::fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(s_tmem, 256);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *s_tmem;
+    const Ctx x = make_ctx(sm, tmem);
+
+    uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
+    uint32_t g_issued = 0, g_done = 0;
+    const int n_items = p.num_seqs * H * p.wn;
+    ItemInfo cur, nxt;
+    int it = blockIdx.x;
+    while (it < n_items && !item_info(p, it, cur)) it += gridDim.x;
+    if (it < n_items) {
+        if (tid == 0) {
+            const int hx = cur.h * D;
+            tma_qk(sm, &tm_q, &tm_k, hx, (int)cur.row0, bar_qk);
+            tma_2box(sm + OFF_Z, &tm_z, hx, (int)cur.row0, bar_z);
+            tma_2box(sm + OFF_V, &tm_v, hx, (int)cur.row0, bar_v);
+        }
+        ++qk_issued; ++z_issued; ++v_issued;
+    }
+    while (it < n_items) {
+        int nit = it + gridDim.x;
+        while (nit < n_items && !item_info(p, nit, nxt)) nit += gridDim.x;
+        const bool has_next = nit < n_items;
+        const int hx = cur.h * D, nhx = has_next ? nxt.h * D : 0;
+        const int nvalid = cur.nvalid;
+        uint8_t *rec = p.records + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * REC_BYTES;
+
+        if (tid < D) x.s_eAn[tid] = -expf(p.A[cur.h * D + tid]) * kLog2e;
+        if (tid < C) x.s_beta[tid] = (tid < nvalid) ? p.beta[(cur.row0 + tid) * H + cur.h] : 0.f;
+        if (tid == 0) ptx::bulk_wait_read();   // the previous item's exports have left smem
+        __syncthreads();
+
+        phase_gate_operands(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
+        ptx::fence_async_smem();
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        if (*s_abort) break;
+        if (tid == 0) {
+            ptx::tc_fence_after_sync();
+            if (has_next) tma_2box(sm + OFF_Z, &tm_z, nhx, (int)nxt.row0, bar_z);
+            mma_k<8>(tmem + TM_G, sbase + OFF_QK, 16384u, sbase + OFF_GB, GB_KBLK,
+                     ptx::idesc_bf16_f32(128, 160), false);
+            ptx::mma_commit(bar_g);
+            bulk_store(rec + REC_B1, sm + OFF_B1, 32768);
+            bulk_store(rec + REC_KE, sm + OFF_KE, 16384);
+            bulk_store(rec + REC_G, reinterpret_cast<const uint8_t *>(x.s_gamma), 512);
+            ptx::bulk_commit();
+        }
+        ++g_issued;
+        if (has_next) ++z_issued;
+
+        if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
+        if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, nhx, (int)nxt.row0, bar_qk);
+        if (has_next) ++qk_issued;
+        if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
+        ptx::tc_fence_after_sync();
+        phase_extract_PL(x, OFF_PB);
+        __syncthreads();
+        phase_diag_and_vt(x, nvalid);
+        ptx::fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            if (has_next) tma_2box(sm + OFF_V, &tm_v, nhx, (int)nxt.row0, bar_v);
+            bulk_store(rec + REC_PB, sm + OFF_PB, 8192);
+            bulk_store(rec + REC_VT, sm + OFF_VT, 16384);
+            ptx::bulk_commit();
+        }
+        if (has_next) ++v_issued;
+        solve_offdiag(x);
+        phase_T(x, OFF_TB_INTRA);
+        ptx::fence_async_smem();
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        if (*s_abort) break;
+        if (tid == 0) {
+            bulk_store(rec + REC_TB, sm + OFF_TB_INTRA, 8192);
+            ptx::bulk_commit();
+        }
+        it = nit;
+        cur = nxt;
+    }
+
+    __syncthreads();
+    if (*s_abort) {
+        if (tid == 0) report_status(p.status, kDevTimeout);
+        while (qk_done < qk_issued && ptx::mbar_wait(bar_qk, qk_done & 1, kWaitBudget)) ++qk_done;
+        while (z_done < z_issued && ptx::mbar_wait(bar_z, z_done & 1, kWaitBudget)) ++z_done;
+        while (v_done < v_issued && ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done;
+        while (g_done < g_issued && ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done;
+    }
+    if (tid == 0) ptx::bulk_wait_all();
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, 256);
+    }
+}
+
+// ---- state-only kernel: shared memory map ------------------------------------
+constexpr uint32_t SB_STAGE = 83968;            // record stage stride (1024-aligned)
+constexpr uint32_t SB_ST = 2 * SB_STAGE - 1024; // 166912: S^T bf16 (after stage 1's 82432 bytes)
+constexpr uint32_t SB_RU = SB_ST + 32768;       // RHS^T / U^T, then the output tile
+constexpr uint32_t SB_BAR = SB_RU + 16384;      // mbarriers and slots
+constexpr uint32_t SMEM_STATE = SB_BAR + 128 + 1024;
+static_assert(SB_STAGE + REC_BYTES <= SB_ST, "stages overlap the state tile");
+static_assert(SMEM_STATE <= 232448, "shared memory budget");
+constexpr uint32_t TS_D1 = 0, TS_D2 = 128, TS_D3 = 256;   // TMEM columns
+
+__global__ void __launch_bounds__(NT, 1)
+prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_addr(sm);
+    uint64_t *bar_st = reinterpret_cast<uint64_t *>(sm + SB_BAR);   // [2] record stages
+    uint64_t *bar_s = bar_st + 2;
+    uint64_t *bar_m = bar_st + 3;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SB_BAR + 64);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + SB_BAR + 72);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int H = p.H;
+    const int chain = blockIdx.x;
+    const int seq = chain / H, h = chain % H;
+    const int hx = h * D;
+    const int64_t rowstride = (int64_t)H * D;
+    const int64_t sidx = (int64_t)chain * D * D;
+    int64_t bos = p.cu_seqlens[seq], eos = p.cu_seqlens[seq + 1];
+    if (bos < 0 || eos < bos || eos > p.total_tokens) bos = eos = 0;   // reported by the intra kernel
+    const int nchunks = (int)((eos - bos + C - 1) / C);
+    const int c_end = (p.w0 + p.wn < nchunks) ? p.w0 + p.wn : nchunks;
+    const bool first = p.w0 == 0;
+    const bool last = p.w0 + p.wn >= nchunks;
+    if (p.w0 >= c_end && !(first && nchunks == 0)) return;   // this chain is done (uniform per CTA)
+
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(bar_st + i, 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&tm_o);
+        *s_abort = 0;
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(s_tmem, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *s_tmem;
+    Ctx x = make_ctx(sm, tmem);
+    const uint8_t *recs = p.records + (size_t)chain * p.W * REC_BYTES;
+
+    uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
+    uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
+    const int c0 = p.w0;
+    if (tid == 0) {
+        for (int k = 0; k < 2; ++k)
+            if (c0 + k < c_end) bulk_load(sm + k * SB_STAGE, recs + (size_t)k * REC_BYTES, REC_BYTES, bar_st + k);
+    }
+    for (int k = 0; k < 2; ++k)
+        if (c0 + k < c_end) ++st_issued[k];
+    const float *src = first ? (p.initial_state ? p.initial_state + sidx : nullptr) : p.states + sidx;
+    load_state(x, src, TS_D3, SB_ST);
+    ptx::fence_async_smem();
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+
+    for (int c = c0; c < c_end; ++c) {
+        const int k = (c - c0) & 1;
+        uint8_t *stg = sm + k * SB_STAGE;
+        const uint32_t sstg = sbase + k * SB_STAGE;
+        const int64_t row0 = bos + (int64_t)c * C;
+        const int nvalid = (int)((eos - row0) < C ? (eos - row0) : C);
+        if (ptx::mbar_wait(bar_st + k, st_done[k] & 1, kWaitBudget)) ++st_done[k]; else *s_abort = 1;
+        if (tid == 0) {
+            ptx::tc_fence_after_sync();
+            // D1[j][s|t] = S^T[j] . [K~;Q~][s|t]
+            mma_k<8>(tmem + TS_D1, sbase + SB_ST, 16384u, sstg + REC_B1, 16384u,
+                     ptx::idesc_bf16_f32(128, 128), false);
+            ptx::mma_commit(bar_s);
+            ptx::bulk_wait_read();   // the previous output tile has left RU
+        }
+        ++s_issued;
+        __syncthreads();
+        if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
+        ptx::tc_fence_after_sync();
+        phase_rhs(x, TS_D1, REC_VT + k * SB_STAGE, SB_RU);
+        ptx::fence_async_smem();
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        if (*s_abort) break;
+        if (tid == 0) {
+            ptx::tc_fence_after_sync();
+            mma_k<4>(tmem + TS_D2, sbase + SB_RU, 0u, sstg + REC_TB, 0u, ptx::idesc_bf16_f32(128, 64), false);
+            ptx::mma_commit(bar_m);
+        }
+        ++m_issued;
+        if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
+        ptx::tc_fence_after_sync();
+        phase_u_scale(x, TS_D2, TS_D3, SB_RU, reinterpret_cast<const float *>(stg + REC_G));
+        ptx::fence_async_smem();
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        if (*s_abort) break;
+        if (tid == 0) {
+            ptx::tc_fence_after_sync();
+            mma_k<4>(tmem + TS_D1 + 64, sbase + SB_RU, 0u, sstg + REC_PB, 0u, ptx::idesc_bf16_f32(128, 64), true);
+            mma_k<4>(tmem + TS_D3, sbase + SB_RU, 0u, sstg + REC_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
+            ptx::mma_commit(bar_m);
+        }
+        ++m_issued;
+        if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
+        ptx::tc_fence_after_sync();
+        phase_state_out(x, TS_D3, TS_D1 + 64, SB_ST, SB_RU);
+        ptx::fence_async_smem();
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        if (*s_abort) break;
+        store_output(x, &tm_o, SB_RU, p.out, row0, nvalid, hx, rowstride);
+        // this stage has been consumed: fetch the record two chunks ahead into it
+        if (tid == 0 && c + 2 < c_end)
+            bulk_load(stg, recs + (size_t)(c + 2 - c0) * REC_BYTES, REC_BYTES, bar_st + k);
+        if (c + 2 < c_end) ++st_issued[k];
+    }
+    if (!*s_abort) {
+        if (last) {
+            if (p.final_state) save_state(x, p.final_state + sidx, TS_D3);
+        } else {
+            save_state(x, p.states + sidx, TS_D3);
+        }
+    }
+    __syncthreads();
+    if (*s_abort) {
+        if (tid == 0) report_status(p.status, kDevTimeout);
+        for (int k = 0; k < 2; ++k)
+            while (st_done[k] < st_issued[k] && ptx::mbar_wait(bar_st + k, st_done[k] & 1, kWaitBudget)) ++st_done[k];
+        while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
+        while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
+    }
+    if (tid == 0) ptx::bulk_wait_all();
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 }  // namespace tc
 
 // ---------------------------------------------------------------------------
-// Host launcher.
+// Host side.
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -768,13 +1239,52 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static int sm_count() {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+// Split-path plan: used when the chains fill at most half the SMs and the
+// sequences average at least 8 chunks.  Workspace after the schedule area:
+// the carried states, then W record slots per chain.
+struct SplitPlan {
+    bool ok;
+    int W;
+    int64_t max_chunks;
+    size_t states_off, records_off, bytes;
+};
+constexpr int kSplitWindow = 256;
+
+static SplitPlan plan_split(int64_t total, int num_seqs, int H) {
+    SplitPlan s{};
+    const int64_t chains = (int64_t)num_seqs * H;
+    s.max_chunks = (total + tc::C - 1) / tc::C;
+    s.ok = chains > 0 && 2 * chains <= sm_count() && total >= (int64_t)8 * tc::C * num_seqs;
+    if (!s.ok) return s;
+    s.W = (int)(s.max_chunks < kSplitWindow ? s.max_chunks : kSplitWindow);
+    const size_t base = (kWsOrder + sizeof(int32_t) * (size_t)num_seqs + 1023) & ~size_t(1023);
+    s.states_off = base;
+    s.records_off = base + (size_t)chains * tc::D * tc::D * sizeof(float);
+    s.bytes = s.records_off + (size_t)chains * s.W * tc::REC_BYTES;
+    return s;
+}
+
+// Extra workspace bytes the tensor-core prefill can use for these sizes (0
+// when the fused kernel alone is planned).
+size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H) {
+    const SplitPlan s = plan_split(total, num_seqs, H);
+    return s.ok ? s.bytes : 0;
+}
+
 cudaError_t launch_schedule(const int32_t *cu, int num_seqs, int32_t *order, uint32_t *counter,
                             uint32_t *status, cudaStream_t st);
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
-                              void *out, void *workspace, cudaStream_t st) {
+                              void *out, void *workspace, size_t workspace_bytes, cudaStream_t st) {
     CUtensorMap mq, mk, mv, mz, mo;
     if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) ||
         !make_map(&mv, v, total, H) || !make_map(&mz, z, total, H) ||
@@ -786,15 +1296,39 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     int32_t *order = reinterpret_cast<int32_t *>(ws + kWsOrder);
     cudaError_t e = launch_schedule(cu, num_seqs, order, counter, status, st);
     if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    const int64_t chains = (int64_t)num_seqs * H;
 
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const SplitPlan plan = plan_split(total, num_seqs, H);
+    if (plan.ok && workspace_bytes >= plan.bytes) {
+        e = cudaFuncSetAttribute(tc::prefill_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc::prefill_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc::SMEM_STATE);
+        if (e != cudaSuccess) return e;
+        tc::SplitParams sp;
+        sp.A = A; sp.beta = beta; sp.cu_seqlens = cu; sp.initial_state = s0; sp.final_state = s1;
+        sp.out = static_cast<__nv_bfloat16 *>(out);
+        sp.records = ws + plan.records_off;
+        sp.states = reinterpret_cast<float *>(ws + plan.states_off);
+        sp.status = status; sp.total_tokens = total; sp.num_seqs = num_seqs; sp.H = H;
+        sp.W = plan.W;
+        for (int64_t w0 = 0; w0 < plan.max_chunks; w0 += plan.W) {
+            sp.w0 = (int)w0;
+            sp.wn = (int)((plan.max_chunks - w0) < plan.W ? (plan.max_chunks - w0) : plan.W);
+            const int64_t items = chains * sp.wn;
+            const int grid = (int)(items < sms ? items : sms);
+            tc::prefill_intra_kernel<<<grid, tc::NT, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mz, sp);
+            tc::prefill_state_kernel<<<(unsigned)chains, tc::NT, tc::SMEM_STATE, st>>>(mo, sp);
+        }
+        return cudaGetLastError();
+    }
+
     e = cudaFuncSetAttribute(tc::prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tc::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    const int64_t n_work = (int64_t)num_seqs * H;
-    const int grid = (int)(n_work < sms ? n_work : sms);
+    const int grid = (int)(chains < sms ? chains : sms);
     tc::Params prm;
     prm.A = A; prm.beta = beta; prm.cu_seqlens = cu; prm.initial_state = s0;
     prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;

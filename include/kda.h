@@ -77,10 +77,16 @@ kda_status_t kda_gate(const void *z, kda_dtype_t z_dtype, const float *A, float 
                       int64_t n_tokens, int H, int dk, kda_stream_t stream);
 
 /*
- * kda_prefill_workspace_size -- bytes of device workspace kda_chunk_prefill
- * needs for these sizes (a few KB: a status word, a work counter and a
- * schedule of num_seqs entries).  The workspace holds no data between calls
- * except the status word, which kda_chunk_prefill clears on entry.
+ * kda_prefill_workspace_size -- bytes of device workspace that let
+ * kda_chunk_prefill use its fastest plan for these sizes.  The minimum it
+ * accepts is 256 + 4 * num_seqs bytes (rounded up to 256): a status word, a
+ * work counter and a schedule.  For bf16, dk = dv = 128 batches with few
+ * (sequence, head) chains (at most half the SM count) the returned size also
+ * holds the chunk-parallel plan's per-chunk records (about 80 KB per chunk of
+ * a window of at most 256 chunks per chain) and one carried state per chain;
+ * with less than that the call falls back to the one-kernel plan.  The
+ * workspace holds no data between calls except the status word, which every
+ * call clears on entry.
  */
 size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
                                   kda_dtype_t dtype);
@@ -99,12 +105,14 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int
  *   final_state    [num_seqs, H, dk, dv] float32 (written), or NULL; it may be
  *                  the same buffer as initial_state
  *   out            [total_tokens, H, dv], element type dtype (written)
- *   workspace      device buffer of at least kda_prefill_workspace_size() bytes,
- *                  16-byte aligned
+ *   workspace      device buffer, 16-byte aligned, of at least the minimum above
+ *                  (kda_prefill_workspace_size() bytes enable every plan)
  * Length-0 sequences copy their initial state (or zeros) to final_state.
- * bf16 inputs with dk = dv = 128 run the chunkwise tensor-core kernel (64-token
- * chunks, 16-token decay tiles); every other supported case runs the
- * token-serial float32 kernel.
+ * bf16 inputs with dk = dv = 128 run the chunkwise tensor-core path (64-token
+ * chunks, 16-token decay tiles): one persistent kernel over the chains when
+ * they fill the GPU, else a chunk-parallel kernel for the state-independent
+ * work followed by a per-chain state-pass kernel.  Every other supported case
+ * runs the token-serial float32 kernel.
  */
 kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,
                                const float *A, const float *beta, const int32_t *cu_seqlens,

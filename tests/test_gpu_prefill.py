@@ -178,3 +178,51 @@ def test_unsupported_and_invalid_arguments():
     with pytest.raises(KDAError):
         chunk_prefill(q, q, q, q, torch.zeros((2, 128), device=dev), torch.zeros((8, 2), device=dev), cu,
                       workspace=ws)
+
+
+def _run_both_paths(d, dev):
+    """The same call with a minimal workspace (the fused kernel) and with the
+    workspace the library asks for (the split path when the batch has few
+    chains)."""
+    from gated_delta_rule_46_gb300 import workspace_size
+    g = to_device(d, dev)
+    T, H, dk = g["q"].shape
+    N = g["cu_seqlens"].shape[0] - 1
+    small = torch.zeros(4096 + 4 * N, dtype=torch.uint8, device=dev)
+    big = torch.zeros(workspace_size(T, N, H, dk, dk), dtype=torch.uint8, device=dev)
+    assert big.numel() > small.numel(), "this batch should plan the split path"
+    args = (g["q"], g["k"], g["v"], g["z"], g["A"], g["beta"], g["cu_seqlens"], g["initial_state"])
+    of, ff = chunk_prefill(*args, workspace=small)
+    os_, fs = chunk_prefill(*args, workspace=big)
+    torch.cuda.synchronize()
+    assert check_device_status(big) == 0 and check_device_status(small) == 0
+    return (of, ff), (os_, fs)
+
+
+def test_split_path_matches_fused_and_oracle():
+    """Few chains, ragged sequences (one empty): the chunk-parallel split path
+    agrees with the oracle and with the fused kernel."""
+    dev = need_gpu()
+    w = inputs.custom([1500, 33, 900, 0, 640, 129], H=4, dk=128, dv=128, dtype=torch.bfloat16,
+                      init="randn0.1", wid=21)
+    d = inputs.prefill_inputs(w)
+    (of, ff), (os_, fs) = _run_both_paths(d, dev)
+    ro, rf = _run_oracle(d)
+    assert_close("split out", os_, ro, torch.bfloat16)
+    assert_close("split final", fs, rf, torch.bfloat16)
+    assert_close("fused out", of, ro, torch.bfloat16)
+    assert_close("split vs fused out", os_, of.double().cpu().numpy(), torch.bfloat16)
+    assert torch.equal(fs[3], d["initial_state"][3].to(dev))   # empty sequence passes its state
+
+
+def test_split_path_several_windows():
+    """A sequence long enough for the split path to run several windows of
+    chunks, carrying the state between them."""
+    dev = need_gpu()
+    w = inputs.custom([20000, 3000], H=2, dk=128, dv=128, dtype=torch.bfloat16, init="randn0.1", wid=22)
+    d = inputs.prefill_inputs(w)
+    (of, ff), (os_, fs) = _run_both_paths(d, dev)
+    ro, rf = _run_oracle(d)
+    assert_close("split out", os_, ro, torch.bfloat16)
+    assert_close("split final", fs, rf, torch.bfloat16)
+    assert_close("fused final", ff, rf, torch.bfloat16)
