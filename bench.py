@@ -344,6 +344,16 @@ def run_gpu(args):
                  "algorithmic_bytes_per_launch": alg_pref, "peak_source": peak_kind,
                  "us_per_launch": per_launch_pref * 1e6}
 
+    # ---- the two large prefill workloads, inputs generated on the device
+    extra = {}
+    if not args.no_extra_workloads:
+        del dsteps, pin_steps, host_steps
+        torch.cuda.empty_cache()
+        for wid in (2, 3):
+            extra[inputs.workload(wid).name] = _time_large_prefill(kda, inputs, wid, dev, seed,
+                                                                   flush, barrier, agg_max, peak,
+                                                                   peak_kind)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pt, dt, cores, sample, _, _, _ = _oracle_sample(budget_s=12.0)
@@ -369,6 +379,7 @@ def run_gpu(args):
             "e2e": {"value": pref_tokens / e2p, "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d_pref + h2d_dec, "d2h_bytes_per_step": d2h_pref + d2h_dec,
                     "decode_value": dec_tokens / e2d},
+            "prefill_large": extra,
             "gpu_launches": K * (3 + NS),
             "clocks": clk.result,
             "device_status": ok_status,
@@ -381,6 +392,63 @@ def run_gpu(args):
     return 0
 
 
+def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, peak, peak_kind,
+                        reps=2):
+    """One KDA layer over the varlen (64 packed sequences) or the 1M-token
+    workload: inputs drawn on the device with the same distributions as the
+    parity inputs (bf16 q/k L2-normalised, v/z N(0,1), beta = sigmoid(N(0,1)),
+    A ~ U(-1,1), zero initial state), outputs and final states written."""
+    import torch
+    w = inputs.workload(wid)
+    T, H, d = w.total_tokens, w.H, w.dk
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + 7 * wid + seed)
+
+    def normal(shape):
+        return torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+
+    q = torch.nn.functional.normalize(normal((T, H, d)), dim=-1).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(normal((T, H, d)), dim=-1).to(torch.bfloat16)
+    v = normal((T, H, d)).to(torch.bfloat16)
+    z = normal((T, H, d)).to(torch.bfloat16)
+    beta = torch.sigmoid(normal((T, H)))
+    A = torch.rand((H, d), generator=g, device=dev) * 2 - 1
+    cu = torch.zeros(len(w.seq_lens) + 1, dtype=torch.int32, device=dev)
+    cu[1:] = torch.cumsum(torch.tensor(w.seq_lens, device=dev), 0)
+    N = len(w.seq_lens)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.zeros(kda.workspace_size(T, N, H, d, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        kda.chunk_prefill(q, k, v, z, A, beta, cu, None, final_state=fin, out=out, workspace=ws)
+
+    call()
+    barrier()
+    times = []
+    for _ in range(reps):
+        flush.fill_(0.5)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        barrier()
+        times.append(e0.elapsed_time(e1) / 1000.0)
+    t = agg_max(min(times))
+    alg = T * H * inputs.bytes_per_token_head(d, d, 2) + N * H * d * d * 4 + H * d * 4 + 4 * (N + 1)
+    ach = alg / t / 1e9
+    status = kda.check_device_status(ws)
+    del q, k, v, z, out, ws
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: {N} seqs, {T} tokens, H={H}, dk=dv={d}, bf16, zero state",
+            "value": T / t, "unit": "tokens/s", "ms_per_call": 1000 * t,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                         "frac": ach / peak, "algorithmic_bytes_per_launch": alg,
+                         "peak_source": peak_kind},
+            "device_status": status}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -388,6 +456,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="skip the varlen and 1M-token prefill measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
