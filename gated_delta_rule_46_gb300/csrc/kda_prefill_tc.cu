@@ -75,7 +75,6 @@ constexpr uint32_t OFF_B1 = 139264;    // [K~; Q~] 128 x 128 bf16 (B of the stat
 constexpr int LSTR = 68;               // float32 row stride of L and Y (16-byte multiple)
 constexpr uint32_t OFF_L = 98304;      // L [64][LSTR] float32
 constexpr uint32_t OFF_Y = OFF_L + 64 * LSTR * 4;      // Y = (I + L)^{-1}
-constexpr uint32_t OFF_W = OFF_Y + 64 * LSTR * 4;      // W_am = Y_aa L_am, 6 blocks of 16 x 16
 constexpr uint32_t OFF_TB = 139264;    // T [t][s]: 64 x 64 bf16 (after the state MMA)
 constexpr uint32_t OFF_RU = 155648;    // RHS^T, then U^T: 128 x 64 bf16 (after the state MMA)
 constexpr uint32_t OFF_KE = 172032;    // Kend^T [c][s] 128 x 64 bf16
@@ -93,7 +92,7 @@ constexpr uint32_t OFF_SLOT = OFF_BAR + 64;          // TMEM base, work item, ab
 constexpr uint32_t SMEM_USED = OFF_SLOT + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // slack to align the base to 1024 B
 static_assert(OFF_GB + 2 * GB_KBLK <= OFF_B1, "right-factor tiles overlap");
-static_assert(OFF_W + 6 * 256 * 4 <= OFF_TB, "solve scratch overlaps");
+static_assert(OFF_Y + 64 * LSTR * 4 <= OFF_TB, "solve scratch overlaps");
 static_assert(OFF_RU + 16384 <= OFF_KE, "RU overlaps");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
@@ -169,32 +168,10 @@ __device__ __forceinline__ void mma_k(uint32_t d, uint32_t a_addr, uint32_t a_kb
     }
 }
 
-// One level of the blocked inverse: Y_ab = -sum_{m=b}^{a-1} W_am Y_mb for the
-// blocks with a - b = dist, where W_am = Y_aa L_am.  One output per task.
-__device__ __forceinline__ void solve_level(int dist, float *Ym, const float *Wm, int tid) {
-    const int ntask = (4 - dist) * 256;
-    for (int task = tid; task < ntask; task += NT) {
-        const int b = task >> 8, a = b + dist, i = (task >> 4) & 15, j = task & 15;
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int m = b; m < a; ++m) {
-            const float *w = Wm + ((a * (a - 1)) / 2 + m) * 256 + i * 16;
-            float wr[16];
-            ld8(w, wr); ld8(w + 8, wr + 8);
-            const float *y = Ym + (16 * m) * LSTR + 16 * b + j;
-#pragma unroll
-            for (int n = 0; n < 16; n += 2) {
-                acc0 += wr[n] * y[n * LSTR];
-                acc1 += wr[n + 1] * y[(n + 1) * LSTR];
-            }
-        }
-        Ym[(16 * a + i) * LSTR + 16 * b + j] = -(acc0 + acc1);
-    }
-}
-
 // Per-thread view of the CTA: shared-memory pointers and the thread's roles.
 struct Ctx {
     uint8_t *sm;
-    float *s_beta, *s_eAn, *s_R, *s_E, *s_rho, *s_tail, *s_gamma, *Lm, *Ym, *Wm;
+    float *s_beta, *s_eAn, *s_R, *s_E, *s_rho, *s_tail, *s_gamma, *Lm, *Ym;
     int tid, warp, lane;
     int qw, cg, ch;        // phases B-D: TMEM lane quarter, column group, value channel j
     int cw, kb, chk;       // phase A: first key channel, its K-block and 16-byte chunk
@@ -213,7 +190,6 @@ __device__ __forceinline__ Ctx make_ctx(uint8_t *sm, uint32_t tmem) {
     x.s_gamma = reinterpret_cast<float *>(sm + OFF_GAMMA);
     x.Lm = reinterpret_cast<float *>(sm + OFF_L);
     x.Ym = reinterpret_cast<float *>(sm + OFF_Y);
-    x.Wm = reinterpret_cast<float *>(sm + OFF_W);
     x.tid = threadIdx.x;
     x.warp = x.tid >> 5;
     x.lane = x.tid & 31;
@@ -446,49 +422,137 @@ __device__ __forceinline__ void phase_diag_and_vt(const Ctx &x, int nvalid) {
     }
 }
 
-// W_am = Y_aa L_am for the six blocks below the diagonal (1 x 4 outputs per task).
-__device__ __forceinline__ void phase_W(const Ctx &x) {
-    const int tid = x.tid;
-    float *Lm = x.Lm;
-    float *Ym = x.Ym;
-    float *Wm = x.Wm;
-    // W_am = Y_aa L_am for the six blocks below the diagonal (1 x 4 outputs per task)
-    for (int task = tid; task < 6 * 64; task += NT) {
-        const int blk = task >> 6, i = (task >> 2) & 15, jj = task & 3;
-        const int a = blk < 1 ? 1 : (blk < 3 ? 2 : 3);
-        const int m = blk - (a * (a - 1)) / 2;
-        float yr[16];
-        const float *src = Ym + (16 * a + i) * LSTR + 16 * a;
-        ld8(src, yr); ld8(src + 8, yr + 8);
+// ---- off-diagonal blocks of the inverse on warp-level tf32 MMAs -------------
+// With D_a = (I + L_aa)^{-1} (the diagonal 16 x 16 blocks, solved above in
+// float32), the blocks below the diagonal follow block-column by block-column:
+//   Y_ab = -D_a sum_{m=b}^{a-1} L_am Y_mb,   Y_bb = D_b.
+// Each of warps 0-5 owns one 8-column half of block column b = warp / 2 and
+// walks a = b+1..3 with m16n8k8 tf32 MMAs (float32 accumulation), keeping the
+// finished blocks of its column in registers; no block barrier is needed.
+__device__ __forceinline__ uint32_t to_tf32(float f) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+    return r;
+}
+// d += a b for one 16 x 8 x 8 tile.
+__device__ __forceinline__ void mma_tf32(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// A operand, k-step ks, of the 16 x 16 block at (r0, c0) of a float32 matrix
+// with row stride LSTR (lane = 4 g + q holds rows g, g + 8 and columns q, q + 4).
+__device__ __forceinline__ void frag_a(const float *M, int r0, int c0, int ks, int g, int q,
+                                       uint32_t *a) {
+    const float *p = M + (r0 + g) * LSTR + c0 + 8 * ks + q;
+    a[0] = to_tf32(p[0]);
+    a[1] = to_tf32(p[8 * LSTR]);
+    a[2] = to_tf32(p[4]);
+    a[3] = to_tf32(p[8 * LSTR + 4]);
+}
+// B operand (both k-steps) of the 16 x 8 block at (r0, n0): rows q, q+4, q+8, q+12, column g.
+__device__ __forceinline__ void frag_b(const float *M, int r0, int n0, int g, int q, uint32_t *b) {
+    const float *p = M + (r0 + q) * LSTR + n0 + g;
+    b[0] = to_tf32(p[0]);
+    b[1] = to_tf32(p[4 * LSTR]);
+    b[2] = to_tf32(p[8 * LSTR]);
+    b[3] = to_tf32(p[12 * LSTR]);
+}
+// A 16 x 8 accumulator (rows g, g+8; columns 2q, 2q+1 per lane) turned into the
+// B operand layout of the next product (rows q, q+4, q+8, q+12; column g).
+__device__ __forceinline__ void c_to_b(const float *c, int lane, uint32_t *b) {
+    const int g = lane >> 2, q = lane & 3;
+    const int s0 = 4 * q + (g >> 1), s1 = s0 + 16;
+    const bool odd = (g & 1) != 0;
+    float e, o;
+    e = __shfl_sync(0xffffffffu, c[0], s0); o = __shfl_sync(0xffffffffu, c[1], s0);
+    b[0] = to_tf32(odd ? o : e);
+    e = __shfl_sync(0xffffffffu, c[0], s1); o = __shfl_sync(0xffffffffu, c[1], s1);
+    b[1] = to_tf32(odd ? o : e);
+    e = __shfl_sync(0xffffffffu, c[2], s0); o = __shfl_sync(0xffffffffu, c[3], s0);
+    b[2] = to_tf32(odd ? o : e);
+    e = __shfl_sync(0xffffffffu, c[2], s1); o = __shfl_sync(0xffffffffu, c[3], s1);
+    b[3] = to_tf32(odd ? o : e);
+}
+
+// Warps 0-5: T_ab = Y_ab Diag(beta) for the blocks below the diagonal, straight
+// into the bf16 T tile [t][s].
+__device__ __forceinline__ void solve_chain(const Ctx &x, uint32_t off_tb) {
+    const int lane = x.lane, g = lane >> 2, q = lane & 3;
+    const int b = x.warp >> 1, n0 = 16 * b + 8 * (x.warp & 1);
+    const float *Lm = x.Lm, *Ym = x.Ym;
+    uint32_t Bm[3][4];   // B operands of Y_mb, m = b + e
+    frag_b(Ym, 16 * b, n0, g, q, Bm[0]);
+    const float bt0 = x.s_beta[n0 + 2 * q], bt1 = x.s_beta[n0 + 2 * q + 1];
+#pragma unroll
+    for (int d = 1; d <= 3; ++d) {
+        const int a = b + d;
+        if (a > 3) break;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            float lv[4];
-            ld4(Lm + (16 * a + n) * LSTR + 16 * m + 4 * jj, lv);
-            acc[0] += yr[n] * lv[0]; acc[1] += yr[n] * lv[1];
-            acc[2] += yr[n] * lv[2]; acc[3] += yr[n] * lv[3];
+        for (int e = 0; e < d; ++e) {
+            uint32_t fa[4];
+            frag_a(Lm, 16 * a, 16 * (b + e), 0, g, q, fa);
+            mma_tf32(acc, fa, Bm[e][0], Bm[e][1]);
+            frag_a(Lm, 16 * a, 16 * (b + e), 1, g, q, fa);
+            mma_tf32(acc, fa, Bm[e][2], Bm[e][3]);
         }
-        *reinterpret_cast<float4 *>(Wm + blk * 256 + i * 16 + 4 * jj) =
-            make_float4(acc[0], acc[1], acc[2], acc[3]);
+        uint32_t bx[4], fa[4];
+        c_to_b(acc, lane, bx);
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        frag_a(Ym, 16 * a, 16 * a, 0, g, q, fa);
+        mma_tf32(y, fa, bx[0], bx[1]);
+        frag_a(Ym, 16 * a, 16 * a, 1, g, q, fa);
+        mma_tf32(y, fa, bx[2], bx[3]);
+        y[0] = -y[0]; y[1] = -y[1]; y[2] = -y[2]; y[3] = -y[3];   // Y_ab
+        const uint32_t col = 4u * q;   // byte offset of column n0 + 2q in its 16-byte chunk
+        *reinterpret_cast<uint32_t *>(x.sm + off_tb + swz(16 * a + g, n0 >> 3) + col) =
+            pack_bf16(y[0] * bt0, y[1] * bt1);
+        *reinterpret_cast<uint32_t *>(x.sm + off_tb + swz(16 * a + g + 8, n0 >> 3) + col) =
+            pack_bf16(y[2] * bt0, y[3] * bt1);
+        if (d < 3) c_to_b(y, lane, Bm[d]);
     }
 }
 
-// T = Y Diag(beta), lower triangle, into its bf16 operand tile; 8 columns per thread.
-__device__ __forceinline__ void phase_T(const Ctx &x, uint32_t off_tb) {
-    uint8_t *sm = x.sm;
-    const int tid = x.tid;
-    float *s_beta = x.s_beta;
-    float *Ym = x.Ym;
-    {
-        // T = Y Diag(beta), lower triangle, bf16; 8 columns per thread
-        const int t = tid >> 3, q8 = tid & 7;
-        float tv[8], yr[8], bv[8];
-        ld8(Ym + t * LSTR + 8 * q8, yr);
-        ld8(s_beta + 8 * q8, bv);
+// Warps 6-7 (one row t each): the diagonal blocks T_aa = D_a Diag(beta) and the
+// zero blocks above the diagonal of the bf16 T tile.
+__device__ __forceinline__ void solve_diag_T(const Ctx &x, uint32_t off_tb) {
+    const int t = x.tid - 6 * 32;
+    const int a = t >> 4;
+    float yr[16], bt[16];
+    const float *src = x.Ym + t * LSTR + 16 * a;
+    ld8(src, yr); ld8(src + 8, yr + 8);
+    ld8(x.s_beta + 16 * a, bt); ld8(x.s_beta + 16 * a + 8, bt + 8);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) tv[i] = (8 * q8 + i <= t) ? yr[i] * bv[i] : 0.f;
-        st_chunk(sm + off_tb, swz(t, q8), tv);
-    }
+    for (int i = 0; i < 16; ++i) yr[i] *= bt[i];
+    st_chunk(x.sm + off_tb, swz(t, 2 * a), yr);
+    st_chunk(x.sm + off_tb, swz(t, 2 * a + 1), yr + 8);
+    for (int c = 2 * a + 2; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(x.sm + off_tb + swz(t, c)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Warps 8-15: RHS^T[j][s] = V^T[j][s] - (K~ S0)^T[j][s], 32 columns per thread.
+__device__ __forceinline__ void phase_rhs_w8(const Ctx &x, uint32_t tm_ks, uint32_t off_vt,
+                                             uint32_t off_ru) {
+    const int half = (x.warp >> 2) & 1;
+    float KS[32], vt[32];
+    ptx::tmem_ld32(x.lane_base + tm_ks + 32 * half, KS);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) ld_chunk(x.sm + off_vt, swz(x.ch, 4 * half + c4), vt + 8 * c4);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) vt[i] -= KS[i];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) st_chunk(x.sm + off_ru, swz(x.ch, 4 * half + c4), vt + 8 * c4);
+}
+
+// After the diagonal blocks: T (warps 0-7) and, in the fused kernel, RHS (warps 8-15).
+__device__ __forceinline__ void solve_T(const Ctx &x, uint32_t off_tb, bool rhs, uint32_t tm_ks,
+                                        uint32_t off_vt, uint32_t off_ru) {
+    if (x.warp < 6) solve_chain(x, off_tb);
+    else if (x.warp < 8) solve_diag_T(x, off_tb);
+    else if (rhs) phase_rhs_w8(x, tm_ks, off_vt, off_ru);
 }
 
 // ---- state-pass pieces shared by the fused and the state-only kernels ------
@@ -637,18 +701,6 @@ __device__ __forceinline__ void tma_2box(uint8_t *dst, const CUtensorMap *tm, in
     ptx::tma_load_2d(dst + 8192, tm, hx + 64, y, bar);
 }
 
-// The blocked inverse after the diagonal blocks: W, then three levels.
-__device__ __forceinline__ void solve_offdiag(const Ctx &x) {
-    phase_W(x);
-    __syncthreads();
-    solve_level(1, x.Ym, x.Wm, x.tid);
-    __syncthreads();
-    solve_level(2, x.Ym, x.Wm, x.tid);
-    __syncthreads();
-    solve_level(3, x.Ym, x.Wm, x.tid);
-    __syncthreads();
-}
-
 // Fused kernel: one CTA per SM, persistent over (sequence, head) chains taken
 // longest-first; every chunk runs phases A-D above.  Used when the batch has
 // enough chains to fill the GPU.
@@ -766,12 +818,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             __syncthreads();
             if (tid == 0 && has_next) tma_2box(sm + OFF_V, &tm_v, hx, (int)next_row, bar_v);
             if (has_next) ++v_issued;
-            solve_offdiag(x);
-            // the state MMA (still reading B1, where T and RHS go) overlapped the solve
+            // the state MMA (still reading B1, where T and RHS go) overlapped the diagonal solve
             if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            phase_T(x, OFF_TB);
-            phase_rhs(x, TM_D1, OFF_VT, OFF_RU);
+            solve_T(x, OFF_TB, true, TM_D1, OFF_VT, OFF_RU);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -1021,8 +1071,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             ptx::bulk_commit();
         }
         if (has_next) ++v_issued;
-        solve_offdiag(x);
-        phase_T(x, OFF_TB_INTRA);
+        solve_T(x, OFF_TB_INTRA, false, 0, 0, 0);
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
