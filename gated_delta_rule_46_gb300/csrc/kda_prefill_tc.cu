@@ -82,11 +82,8 @@ constexpr uint32_t OFF_ST = 188416;    // S^T [j][c] 128 x 128 bf16 (A of the st
 constexpr uint32_t OFF_MISC = 221184;
 constexpr uint32_t OFF_BETA = OFF_MISC;              // 64 float
 constexpr uint32_t OFF_EAN = OFF_BETA + 256;         // 128 float: -exp(A) log2(e)
-constexpr uint32_t OFF_R = OFF_EAN + 512;            // [4][128]: R1, R2, R3, G_end (log2 units)
-constexpr uint32_t OFF_E = OFF_R + 2048;             // [4][128]: 2^(R_{a+1} - R_a)
-constexpr uint32_t OFF_RHO = OFF_E + 2048;           // [4][128]: 2^(R_a)
-constexpr uint32_t OFF_TAIL = OFF_RHO + 2048;        // [4][128]: prod_{a' > a} E_a'
-constexpr uint32_t OFF_GAMMA = OFF_TAIL + 2048;      // 128 float: 2^(G_end)
+constexpr uint32_t OFF_HT = OFF_EAN + 512;           // [8][128]: half-tile sums of the log2 decay
+constexpr uint32_t OFF_GAMMA = OFF_HT + 4096;        // 128 float: 2^(G_end)
 constexpr uint32_t OFF_BAR = OFF_GAMMA + 512;        // mbarriers
 constexpr uint32_t OFF_SLOT = OFF_BAR + 64;          // TMEM base, work item, abort flag
 constexpr uint32_t SMEM_USED = OFF_SLOT + 64;
@@ -171,10 +168,9 @@ __device__ __forceinline__ void mma_k(uint32_t d, uint32_t a_addr, uint32_t a_kb
 // Per-thread view of the CTA: shared-memory pointers and the thread's roles.
 struct Ctx {
     uint8_t *sm;
-    float *s_beta, *s_eAn, *s_R, *s_E, *s_rho, *s_tail, *s_gamma, *Lm, *Ym;
+    float *s_beta, *s_eAn, *s_ht, *s_gamma, *Lm, *Ym;
     int tid, warp, lane;
     int qw, cg, ch;        // phases B-D: TMEM lane quarter, column group, value channel j
-    int cw, kb, chk;       // phase A: first key channel, its K-block and 16-byte chunk
     uint32_t lane_base;    // TMEM address of this warp's lane quarter
 };
 
@@ -183,10 +179,7 @@ __device__ __forceinline__ Ctx make_ctx(uint8_t *sm, uint32_t tmem) {
     x.sm = sm;
     x.s_beta = reinterpret_cast<float *>(sm + OFF_BETA);
     x.s_eAn = reinterpret_cast<float *>(sm + OFF_EAN);
-    x.s_R = reinterpret_cast<float *>(sm + OFF_R);
-    x.s_E = reinterpret_cast<float *>(sm + OFF_E);
-    x.s_rho = reinterpret_cast<float *>(sm + OFF_RHO);
-    x.s_tail = reinterpret_cast<float *>(sm + OFF_TAIL);
+    x.s_ht = reinterpret_cast<float *>(sm + OFF_HT);
     x.s_gamma = reinterpret_cast<float *>(sm + OFF_GAMMA);
     x.Lm = reinterpret_cast<float *>(sm + OFF_L);
     x.Ym = reinterpret_cast<float *>(sm + OFF_Y);
@@ -196,139 +189,112 @@ __device__ __forceinline__ Ctx make_ctx(uint8_t *sm, uint32_t tmem) {
     x.qw = x.warp & 3;
     x.cg = x.warp >> 2;
     x.ch = 32 * x.qw + x.lane;
-    x.cw = 8 * x.warp;
-    x.kb = x.warp >> 3;
-    x.chk = x.warp & 7;
     x.lane_base = tmem + ((uint32_t)(32 * x.qw) << 16);
     return x;
 }
 
-// Phase A of a chunk: bounded gate and log2-domain cumulative decay (rows lane
-// and lane + 32, 8 key channels per warp; scans over the lanes), the 16-token
-// tile references and their factors, and the operand tiles: [Q^; K^] in place
-// over the q/k tiles, the right factors of the four Gram/P tiles, [K~; Q~] and
-// Kend^T.  Waits for the z and q/k tiles itself.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+
+// Phase A of a chunk: bounded gate, log2-domain cumulative decay and the
+// operand tiles.  Thread (warp w, lane l) owns key channels c = 64 (w >> 3) + 2l
+// and c + 1 of the eight rows 8h .. 8h + 7, h = w & 7 (the first or second half
+// of 16-token tile h / 2): the scan runs in registers, the eight half-tile sums
+// per channel are exchanged through shared memory, and every operand row is
+// written with 4-byte stores (one 128-byte row segment per warp).  Builds
+// [Q^; K^] in place over the q/k tiles, the right factors of the four Gram/P
+// tiles, [K~; Q~] and Kend^T, and 2^(G_end).  Waits for the z and q/k tiles
+// itself.
 __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, uint64_t *bar_z,
                                                     uint32_t &z_done, uint64_t *bar_qk,
                                                     uint32_t &qk_done, volatile int *s_abort) {
     uint8_t *sm = x.sm;
-    const int lane = x.lane, cw = x.cw, kb = x.kb, chk = x.chk;
-    float *s_eAn = x.s_eAn;
-    float *s_R = x.s_R;
-    float *s_E = x.s_E;
-    float *s_rho = x.s_rho;
-    float *s_tail = x.s_tail;
-    float *s_gamma = x.s_gamma;
+    const int lane = x.lane, h = x.warp & 7, kb = x.warp >> 3;
+    const int ta = h >> 1;                          // 16-token tile of these rows
+    const int c = 64 * kb + 2 * lane;               // first of the two key channels
+    const uint32_t cb = (uint32_t)(lane >> 2);      // 16-byte chunk of the channels in a row
+    const uint32_t co = (uint32_t)(lane & 3) * 4u;  // byte offset inside that chunk
+    float *s_ht = x.s_ht;                           // [8][128] half-tile sums (log2 units)
+    const float2 ea = *reinterpret_cast<const float2 *>(x.s_eAn + c);
     if (ptx::mbar_wait(bar_z, z_done & 1, kWaitBudget)) ++z_done; else *s_abort = 1;
-    float G0[8], G1[8];   // log2-domain cumulative log-decay of rows lane, lane + 32
+    // g = g_min sigmoid(exp(A) z) = g_min / (1 + 2^(-exp(A) z log2 e)), rows past the end 0;
+    // inclusive sums over this thread's eight rows
+    float g0[8], g1[8];
     {
-        float z0[8], z1[8], eAn[8];
         const uint8_t *zt = sm + OFF_Z + kb * 8192;
-        ld_chunk(zt, swz(lane, chk), z0);
-        ld_chunk(zt, swz(lane + 32, chk), z1);
-        ld8(s_eAn + cw, eAn);
-        const bool ok0 = lane < nvalid, ok1 = lane + 32 < nvalid;
+        float run0 = 0.f, run1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            // g = g_min sigmoid(exp(A) z) = g_min / (1 + 2^(-exp(A) z log2 e))
-            float a0 = ok0 ? kGMin2 * rcp(1.f + ex2(eAn[i] * z0[i])) : 0.f;
-            float a1 = ok1 ? kGMin2 * rcp(1.f + ex2(eAn[i] * z1[i])) : 0.f;
-            // inclusive scans over the lanes: rows 0..31, then rows 32..63
+            const int t = 8 * h + i;
+            const float2 zz = bf2_to_f2(*reinterpret_cast<const uint32_t *>(zt + swz(t, cb) + co));
+            const bool ok = t < nvalid;
+            run0 += ok ? kGMin2 * rcp(1.f + ex2(ea.x * zz.x)) : 0.f;
+            run1 += ok ? kGMin2 * rcp(1.f + ex2(ea.y * zz.y)) : 0.f;
+            g0[i] = run0;
+            g1[i] = run1;
+        }
+        *reinterpret_cast<float2 *>(s_ht + h * 128 + c) = make_float2(run0, run1);
+    }
+    __syncthreads();
+    // R_a (start of tile a), G_end = R_4, and the first half of this tile when h is odd
+    float R0[5], R1[5], hp0 = 0.f, hp1 = 0.f;
+    {
+        float acc0 = 0.f, acc1 = 0.f;
+        R0[0] = 0.f;
+        R1[0] = 0.f;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float t0 = __shfl_up_sync(0xffffffffu, a0, off);
-                const float t1 = __shfl_up_sync(0xffffffffu, a1, off);
-                if (lane >= off) { a0 += t0; a1 += t1; }
-            }
-            G0[i] = a0;
-            G1[i] = a1 + __shfl_sync(0xffffffffu, a0, 31);
+        for (int hh = 0; hh < 8; ++hh) {
+            const float2 v = *reinterpret_cast<const float2 *>(s_ht + hh * 128 + c);
+            if (hh + 1 == h && (h & 1)) { hp0 = v.x; hp1 = v.y; }
+            acc0 += v.x;
+            acc1 += v.y;
+            if (hh & 1) { R0[(hh >> 1) + 1] = acc0; R1[(hh >> 1) + 1] = acc1; }
         }
     }
-    // tile references: rows 15, 31, 47, 63 live in lanes 15 (G0), 31 (G0), 15 (G1), 31 (G1)
-    if ((lane & 15) == 15) {
-        float *d0 = s_R + (lane >> 4) * 128 + cw;          // R1 or R2
-        float *d1 = s_R + (2 + (lane >> 4)) * 128 + cw;    // R3 or G_end
-        *reinterpret_cast<float4 *>(d0) = make_float4(G0[0], G0[1], G0[2], G0[3]);
-        *reinterpret_cast<float4 *>(d0 + 4) = make_float4(G0[4], G0[5], G0[6], G0[7]);
-        *reinterpret_cast<float4 *>(d1) = make_float4(G1[0], G1[1], G1[2], G1[3]);
-        *reinterpret_cast<float4 *>(d1 + 4) = make_float4(G1[4], G1[5], G1[6], G1[7]);
-    }
-    __syncwarp();
-    if (lane < 8) {
-        const int c = cw + lane;
-        const float R1 = s_R[c], R2 = s_R[128 + c], R3 = s_R[256 + c], Ge = s_R[384 + c];
-        const float E0 = ex2(R1), E1 = ex2(R2 - R1), E2 = ex2(R3 - R2), E3 = ex2(Ge - R3);
-        s_E[c] = E0; s_E[128 + c] = E1; s_E[256 + c] = E2; s_E[384 + c] = E3;
-        s_rho[c] = 1.f; s_rho[128 + c] = ex2(R1); s_rho[256 + c] = ex2(R2);
-        s_rho[384 + c] = ex2(R3);
-        s_tail[c] = E1 * E2 * E3; s_tail[128 + c] = E2 * E3; s_tail[256 + c] = E3;
-        s_tail[384 + c] = 1.f;
-        s_gamma[c] = ex2(Ge);
+    const float Rt0 = ta == 0 ? 0.f : ta == 1 ? R0[1] : ta == 2 ? R0[2] : R0[3];
+    const float Rt1 = ta == 0 ? 0.f : ta == 1 ? R1[1] : ta == 2 ? R1[2] : R1[3];
+    if (h == 0) *reinterpret_cast<float2 *>(x.s_gamma + c) = make_float2(ex2(R0[4]), ex2(R1[4]));
+    const float rho0 = ex2(Rt0), rho1 = ex2(Rt1);                 // 2^(R_ta)
+    const float ke0 = ex2(R0[4] - Rt0), ke1 = ex2(R1[4] - Rt1);   // 2^(G_end - R_ta)
+    float f0[4], f1[4];                                           // 2^(R_a2 - R_ta), a2 >= ta
+#pragma unroll
+    for (int a2 = 0; a2 < 4; ++a2) {
+        f0[a2] = a2 > ta ? ex2(R0[a2] - Rt0) : 1.f;
+        f1[a2] = a2 > ta ? ex2(R1[a2] - Rt1) : 1.f;
     }
     if (ptx::mbar_wait(bar_qk, qk_done & 1, kWaitBudget)) ++qk_done; else *s_abort = 1;
-    __syncwarp();
-    {
-        const uint32_t kbo = kb * 16384;
-        const uint32_t gbk = OFF_GB + kb * GB_KBLK;
+    uint8_t *qk = sm + OFF_QK + kb * 16384;
+    uint8_t *b1 = sm + OFF_B1 + kb * 16384;
+    uint8_t *gb = sm + OFF_GB + kb * GB_KBLK;
+    float kr0[8], kr1[8];   // Kend^T rows c and c + 1, columns 8h .. 8h + 7
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int r = lane + 32 * rr;
-            const int ta = r >> 4;                       // 16-token tile of this row
-            const bool ok = r < nvalid;
-            float Rb[8], rho[8], E[8], tl[8];
-            if (ta == 0) {
+    for (int i = 0; i < 8; ++i) {
+        const int t = 8 * h + i;
+        const bool ok = t < nvalid;
+        const uint32_t oq = swz(t, cb) + co, okk = swz(64 + t, cb) + co;
+        const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qk + oq));
+        const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qk + okk));
+        const float x0 = hp0 + g0[i], x1 = hp1 + g1[i];   // G_t - R_ta, in (-115.4, 0]
+        const float el0 = ok ? ex2(x0) : 0.f, el1 = ok ? ex2(x1) : 0.f;     // left factors
+        const float dd0 = ok ? ex2(-x0) : 0.f, dd1 = ok ? ex2(-x1) : 0.f;   // right factors
+        const float qe0 = qv.x * el0, qe1 = qv.y * el1, kh0 = kv.x * el0, kh1 = kv.y * el1;
+        *reinterpret_cast<uint32_t *>(qk + oq) = pack_bf16(qe0, qe1);        // [Q^; K^] in place
+        *reinterpret_cast<uint32_t *>(qk + okk) = pack_bf16(kh0, kh1);
+        *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kh0 * rho0, kh1 * rho1);    // K~
+        *reinterpret_cast<uint32_t *>(b1 + okk) = pack_bf16(qe0 * rho0, qe1 * rho1);   // Q~
+        const float fr0 = kv.x * dd0, fr1 = kv.y * dd1;                     // k 2^(R_ta - G_t)
+        kr0[i] = fr0 * ke0;                                                 // k 2^(G_end - G_t)
+        kr1[i] = fr1 * ke1;
+        // right factors for the Gram/P tiles a2 >= ta: k 2^(R_a2 - G_t)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) Rb[i] = 0.f;
-            } else {
-                ld8(s_R + (ta - 1) * 128 + cw, Rb);
-            }
-            ld8(s_rho + ta * 128 + cw, rho);
-            ld8(s_E + ta * 128 + cw, E);
-            ld8(s_tail + ta * 128 + cw, tl);
-            float qv[8], kv[8];
-            ld_chunk(sm + OFF_QK + kbo, swz(r, chk), qv);
-            ld_chunk(sm + OFF_QK + kbo, swz(64 + r, chk), kv);
-            float qe[8], ke[8], f[8], tk[8], tq[8], kend[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float x = (rr ? G1[i] : G0[i]) - Rb[i];   // in (-115.4, 0]
-                const float el = ok ? ex2(x) : 0.f;              // left factor
-                const float dd = ok ? ex2(-x) : 0.f;             // right factor
-                qe[i] = qv[i] * el;
-                ke[i] = kv[i] * el;
-                f[i] = kv[i] * dd;
-                tk[i] = ke[i] * rho[i];
-                tq[i] = qe[i] * rho[i];
-                kend[i] = (f[i] * E[i]) * tl[i];                 // k 2^(G_end - G_r)
-            }
-            st_chunk(sm + OFF_QK + kbo, swz(r, chk), qe);        // in place: [Q^; K^]
-            st_chunk(sm + OFF_QK + kbo, swz(64 + r, chk), ke);
-            st_chunk(sm + OFF_B1 + kbo, swz(r, chk), tk);
-            st_chunk(sm + OFF_B1 + kbo, swz(64 + r, chk), tq);
-            // Kend^T [c][s]
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int c = cw + i;
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_KE + swz(c, r >> 3) + (r & 7) * 2) =
-                    __float2bfloat16_rn(kend[i]);
-            }
-            // right factors for the Gram/P tiles a2 >= ta: k 2^(R_a2 - G_r)
-            for (int a2 = ta; a2 < 4; ++a2) {
-                st_chunk(sm + gbk, swz(tile_off(a2) + r, chk), f);
-                if (a2 < 3) {   // next tile: multiply by E_a2 = 2^(R_{a2+1} - R_a2)
-                    float en[8];
-                    if (a2 == ta) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) en[i] = E[i];
-                    } else {
-                        ld8(s_E + a2 * 128 + cw, en);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) f[i] *= en[i];
-                }
-            }
-        }
+        for (int a2 = 0; a2 < 4; ++a2)
+            if (a2 >= ta)
+                *reinterpret_cast<uint32_t *>(gb + swz(tile_off(a2) + t, cb) + co) =
+                    pack_bf16(fr0 * f0[a2], fr1 * f1[a2]);
     }
+    st_chunk(sm + OFF_KE, swz(c, h), kr0);
+    st_chunk(sm + OFF_KE, swz(c + 1, h), kr1);
 }
 
 // P (TMEM rows 0..63 of the Gram/P accumulator) and L (rows 64..127), masked
