@@ -45,6 +45,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -79,6 +81,7 @@ constexpr uint32_t OFF_TB = 139264;    // T [t][s]: 64 x 64 bf16 (after the stat
 constexpr uint32_t OFF_RU = 155648;    // RHS^T, then U^T: 128 x 64 bf16 (after the state MMA)
 constexpr uint32_t OFF_KE = 172032;    // Kend^T [c][s] 128 x 64 bf16
 constexpr uint32_t OFF_ST = 188416;    // S^T [j][c] 128 x 128 bf16 (A of the state MMA)
+constexpr uint32_t OFF_KT = OFF_ST + 8192;   // intra kernel only: K~^T [c][s] 128 x 64 bf16
 constexpr uint32_t OFF_MISC = 221184;
 constexpr uint32_t OFF_BETA = OFF_MISC;              // 64 float
 constexpr uint32_t OFF_EAN = OFF_BETA + 256;         // 128 float: -exp(A) log2(e)
@@ -206,6 +209,7 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
 // [Q^; K^] in place over the q/k tiles, the right factors of the four Gram/P
 // tiles, [K~; Q~] and Kend^T, and 2^(G_end).  Waits for the z and q/k tiles
 // itself.
+template <bool KT>
 __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, uint64_t *bar_z,
                                                     uint32_t &z_done, uint64_t *bar_qk,
                                                     uint32_t &qk_done, volatile int *s_abort) {
@@ -268,6 +272,7 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
     uint8_t *b1 = sm + OFF_B1 + kb * 16384;
     uint8_t *gb = sm + OFF_GB + kb * GB_KBLK;
     float kr0[8], kr1[8];   // Kend^T rows c and c + 1, columns 8h .. 8h + 7
+    float kt0[8], kt1[8];   // K~^T rows c and c + 1 (KT only)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int t = 8 * h + i;
@@ -281,7 +286,9 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
         const float qe0 = qv.x * el0, qe1 = qv.y * el1, kh0 = kv.x * el0, kh1 = kv.y * el1;
         *reinterpret_cast<uint32_t *>(qk + oq) = pack_bf16(qe0, qe1);        // [Q^; K^] in place
         *reinterpret_cast<uint32_t *>(qk + okk) = pack_bf16(kh0, kh1);
-        *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kh0 * rho0, kh1 * rho1);    // K~
+        kt0[i] = kh0 * rho0;
+        kt1[i] = kh1 * rho1;
+        *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kt0[i], kt1[i]);            // K~
         *reinterpret_cast<uint32_t *>(b1 + okk) = pack_bf16(qe0 * rho0, qe1 * rho1);   // Q~
         const float fr0 = kv.x * dd0, fr1 = kv.y * dd1;                     // k 2^(R_ta - G_t)
         kr0[i] = fr0 * ke0;                                                 // k 2^(G_end - G_t)
@@ -295,6 +302,10 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
     }
     st_chunk(sm + OFF_KE, swz(c, h), kr0);
     st_chunk(sm + OFF_KE, swz(c + 1, h), kr1);
+    if (KT) {
+        st_chunk(sm + OFF_KT, swz(c, h), kt0);
+        st_chunk(sm + OFF_KT, swz(c + 1, h), kt1);
+    }
 }
 
 // P (TMEM rows 0..63 of the Gram/P accumulator) and L (rows 64..127), masked
@@ -340,61 +351,66 @@ __device__ __forceinline__ void phase_extract_PL(const Ctx &x, uint32_t off_pb) 
 }
 
 // Warps 0-3: the four diagonal 16 x 16 blocks of (I + L)^{-1} by forward
-// substitution (one column per lane); the other warps meanwhile transpose the
-// v tile into V^T [j][s], rows past the sequence end zeroed.
-__device__ __forceinline__ void phase_diag_and_vt(const Ctx &x, int nvalid) {
-    uint8_t *sm = x.sm;
+// substitution in float32 (one column per lane).
+__device__ __forceinline__ void phase_diag(const Ctx &x) {
     const int warp = x.warp, lane = x.lane;
     float *Lm = x.Lm;
     float *Ym = x.Ym;
-    if (warp < 4) {
-        // diagonal 16 x 16 blocks of (I + L)^{-1} by forward substitution, one column per lane
-        if (lane < 16) {
-            const int b0 = 16 * warp;
-            float y[16];
+    if (warp < 4 && lane < 16) {
+        const int b0 = 16 * warp;
+        float y[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float lr[16];
-                const float *src = Lm + (b0 + i) * LSTR + b0;
-                ld8(src, lr); ld8(src + 8, lr + 8);
-                float a0 = (i == lane) ? 1.f : 0.f, a1 = 0.f;
+        for (int i = 0; i < 16; ++i) {
+            float lr[16];
+            const float *src = Lm + (b0 + i) * LSTR + b0;
+            ld8(src, lr); ld8(src + 8, lr + 8);
+            float a0 = (i == lane) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-                for (int mm = 0; mm < i; ++mm) {
-                    if (mm & 1) a1 -= lr[mm] * y[mm]; else a0 -= lr[mm] * y[mm];
-                }
-                y[i] = a0 + a1;
+            for (int mm = 0; mm < i; ++mm) {
+                if (mm & 1) a1 -= lr[mm] * y[mm]; else a0 -= lr[mm] * y[mm];
             }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Ym[(b0 + i) * LSTR + b0 + lane] = y[i];
+            y[i] = a0 + a1;
         }
-    } else {
-        // meanwhile: V^T [j][s] (rows past the sequence end zeroed); a warp
-        // transposes one 8-channel chunk, lane = rows lane and lane + 32
-        for (int cc = warp - 4; cc < 16; cc += 12) {
-            float v0[8], v1[8];
-            const uint8_t *vt = sm + OFF_V + (cc >> 3) * 8192;
-            ld_chunk(vt, swz(lane, cc & 7), v0);
-            ld_chunk(vt, swz(lane + 32, cc & 7), v1);
-            const bool ok0 = lane < nvalid, ok1 = lane + 32 < nvalid;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = 8 * cc + i;
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, lane >> 3) + (lane & 7) * 2) =
-                    __float2bfloat16_rn(ok0 ? v0[i] : 0.f);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, 4 + (lane >> 3)) + (lane & 7) * 2) =
-                    __float2bfloat16_rn(ok1 ? v1[i] : 0.f);
-            }
+        for (int i = 0; i < 16; ++i) Ym[(b0 + i) * LSTR + b0 + lane] = y[i];
+    }
+}
+
+// Warps 1-15 (warp 0 issues the MMAs meanwhile): V^T [j][s] from the v tile,
+// rows past the sequence end zeroed; a warp transposes one 8-channel chunk, lane
+// = rows lane and lane + 32.
+__device__ __forceinline__ void phase_vt(const Ctx &x, int nvalid) {
+    uint8_t *sm = x.sm;
+    const int lane = x.lane;
+    for (int cc = x.warp - 1; cc >= 0 && cc < 16; cc += 15) {
+        float v0[8], v1[8];
+        const uint8_t *vt = sm + OFF_V + (cc >> 3) * 8192;
+        ld_chunk(vt, swz(lane, cc & 7), v0);
+        ld_chunk(vt, swz(lane + 32, cc & 7), v1);
+        const bool ok0 = lane < nvalid, ok1 = lane + 32 < nvalid;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int j = 8 * cc + i;
+            *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, lane >> 3) + (lane & 7) * 2) =
+                __float2bfloat16_rn(ok0 ? v0[i] : 0.f);
+            *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_VT + swz(j, 4 + (lane >> 3)) + (lane & 7) * 2) =
+                __float2bfloat16_rn(ok1 ? v1[i] : 0.f);
         }
     }
 }
 
 // ---- off-diagonal blocks of the inverse on warp-level tf32 MMAs -------------
-// With D_a = (I + L_aa)^{-1} (the diagonal 16 x 16 blocks, solved above in
-// float32), the blocks below the diagonal follow block-column by block-column:
-//   Y_ab = -D_a sum_{m=b}^{a-1} L_am Y_mb,   Y_bb = D_b.
-// Each of warps 0-5 owns one 8-column half of block column b = warp / 2 and
-// walks a = b+1..3 with m16n8k8 tf32 MMAs (float32 accumulation), keeping the
-// finished blocks of its column in registers; no block barrier is needed.
+// With D_a = (I + L_aa)^{-1} (the diagonal 16 x 16 blocks, solved before in
+// float32), the blocks below the diagonal follow block column by block column,
+//   Y_ab = -D_a sum_{m=b}^{a-1} L_am Y_mb,   Y_bb = D_b,
+// computed here transposed, Z_ab = Y_ab^T = -(sum_m Z_mb L_am^T) D_a^T, so that
+// every product's accumulator is the next product's left operand.  Warp b
+// (0-2) walks a = b+1..3 with m16n8k8 tf32 MMAs (float32 accumulation) and
+// keeps its column's blocks in registers.  The accumulator holds columns
+// 2q, 2q+1 of a k-step where the left operand wants q, q+4, so the reduction
+// index of every product is permuted that way (k <-> 2k, k+4 <-> 2k+1 within
+// each k-step) and the right operands, read from shared memory, use the same
+// order.
 __device__ __forceinline__ uint32_t to_tf32(float f) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
@@ -407,84 +423,107 @@ __device__ __forceinline__ void mma_tf32(float *d, const uint32_t *a, uint32_t b
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// A operand, k-step ks, of the 16 x 16 block at (r0, c0) of a float32 matrix
-// with row stride LSTR (lane = 4 g + q holds rows g, g + 8 and columns q, q + 4).
-__device__ __forceinline__ void frag_a(const float *M, int r0, int c0, int ks, int g, int q,
-                                       uint32_t *a) {
-    const float *p = M + (r0 + g) * LSTR + c0 + 8 * ks + q;
-    a[0] = to_tf32(p[0]);
-    a[1] = to_tf32(p[8 * LSTR]);
-    a[2] = to_tf32(p[4]);
-    a[3] = to_tf32(p[8 * LSTR + 4]);
+// Right operand of k-step ks, n-tile nt, for B[k][n] = M[r0 + 8 nt + n][c0 + k] (a
+// transposed 16 x 16 block of a float32 matrix with row stride LSTR), permuted k.
+__device__ __forceinline__ void frag_bt(const float *M, int r0, int c0, int nt, int ks, int g,
+                                        int q, uint32_t &b0, uint32_t &b1) {
+    const float2 v = *reinterpret_cast<const float2 *>(M + (r0 + 8 * nt + g) * LSTR + c0 + 8 * ks + 2 * q);
+    b0 = to_tf32(v.x);
+    b1 = to_tf32(v.y);
 }
-// B operand (both k-steps) of the 16 x 8 block at (r0, n0): rows q, q+4, q+8, q+12, column g.
-__device__ __forceinline__ void frag_b(const float *M, int r0, int n0, int g, int q, uint32_t *b) {
-    const float *p = M + (r0 + q) * LSTR + n0 + g;
-    b[0] = to_tf32(p[0]);
-    b[1] = to_tf32(p[4 * LSTR]);
-    b[2] = to_tf32(p[8 * LSTR]);
-    b[3] = to_tf32(p[12 * LSTR]);
+// 16 x 16 accumulator (two n-tiles) -> left operand of both k-steps, permuted k.
+__device__ __forceinline__ void acc_to_a(const float (*c)[4], uint32_t (*a)[4]) {
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        a[ks][0] = to_tf32(c[ks][0]);
+        a[ks][1] = to_tf32(c[ks][2]);
+        a[ks][2] = to_tf32(c[ks][1]);
+        a[ks][3] = to_tf32(c[ks][3]);
+    }
 }
-// A 16 x 8 accumulator (rows g, g+8; columns 2q, 2q+1 per lane) turned into the
-// B operand layout of the next product (rows q, q+4, q+8, q+12; column g).
-__device__ __forceinline__ void c_to_b(const float *c, int lane, uint32_t *b) {
-    const int g = lane >> 2, q = lane & 3;
-    const int s0 = 4 * q + (g >> 1), s1 = s0 + 16;
-    const bool odd = (g & 1) != 0;
-    float e, o;
-    e = __shfl_sync(0xffffffffu, c[0], s0); o = __shfl_sync(0xffffffffu, c[1], s0);
-    b[0] = to_tf32(odd ? o : e);
-    e = __shfl_sync(0xffffffffu, c[0], s1); o = __shfl_sync(0xffffffffu, c[1], s1);
-    b[1] = to_tf32(odd ? o : e);
-    e = __shfl_sync(0xffffffffu, c[2], s0); o = __shfl_sync(0xffffffffu, c[3], s0);
-    b[2] = to_tf32(odd ? o : e);
-    e = __shfl_sync(0xffffffffu, c[2], s1); o = __shfl_sync(0xffffffffu, c[3], s1);
-    b[3] = to_tf32(odd ? o : e);
+// acc += Z A-operand x (L_{ar} block)^T, for both n-tiles.
+__device__ __forceinline__ void mma_zlt(float (*acc)[4], const uint32_t (*za)[4], const float *Lm,
+                                        int a, int m, int g, int q) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t b0, b1;
+            frag_bt(Lm, 16 * a, 16 * m, nt, ks, g, q, b0, b1);
+            mma_tf32(acc[nt], za[ks], b0, b1);
+        }
 }
 
-// Warps 0-5: T_ab = Y_ab Diag(beta) for the blocks below the diagonal, straight
-// into the bf16 T tile [t][s].
+// Warps 0-2: T_ab = Y_ab Diag(beta) for the blocks below the diagonal in block
+// column b = warp, straight into the bf16 T tile [t][s].
 __device__ __forceinline__ void solve_chain(const Ctx &x, uint32_t off_tb) {
     const int lane = x.lane, g = lane >> 2, q = lane & 3;
-    const int b = x.warp >> 1, n0 = 16 * b + 8 * (x.warp & 1);
+    const int b = x.warp;
     const float *Lm = x.Lm, *Ym = x.Ym;
-    uint32_t Bm[3][4];   // B operands of Y_mb, m = b + e
-    frag_b(Ym, 16 * b, n0, g, q, Bm[0]);
-    const float bt0 = x.s_beta[n0 + 2 * q], bt1 = x.s_beta[n0 + 2 * q + 1];
+    uint32_t za[3][2][4];     // left operands of Z_{b+e, b}, e = 0..2
+    float acc[3][2][4];       // sum_m Z_mb L_am^T for a = b+1..b+3
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {   // Z_bb = D_b^T
+        const float *p = Ym + (16 * b + 8 * ks + 2 * q) * LSTR + 16 * b + g;
+        za[0][ks][0] = to_tf32(p[0]);
+        za[0][ks][1] = to_tf32(p[8]);
+        za[0][ks][2] = to_tf32(p[LSTR]);
+        za[0][ks][3] = to_tf32(p[LSTR + 8]);
+    }
+#pragma unroll
+    for (int d = 0; d < 3; ++d)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[d][nt][i] = 0.f;
+#pragma unroll
+    for (int d = 1; d <= 3; ++d)
+        if (b + d <= 3) mma_zlt(acc[d - 1], za[0], Lm, b + d, b, g, q);
+    const float bt0 = x.s_beta[16 * b + g], bt1 = x.s_beta[16 * b + g + 8];
 #pragma unroll
     for (int d = 1; d <= 3; ++d) {
         const int a = b + d;
         if (a > 3) break;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // Z_ab = -acc D_a^T
+        uint32_t xa[2][4];
+        acc_to_a(acc[d - 1], xa);
+        float z[2][4];
 #pragma unroll
-        for (int e = 0; e < d; ++e) {
-            uint32_t fa[4];
-            frag_a(Lm, 16 * a, 16 * (b + e), 0, g, q, fa);
-            mma_tf32(acc, fa, Bm[e][0], Bm[e][1]);
-            frag_a(Lm, 16 * a, 16 * (b + e), 1, g, q, fa);
-            mma_tf32(acc, fa, Bm[e][2], Bm[e][3]);
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) z[nt][i] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t b0, b1;
+                frag_bt(Ym, 16 * a, 16 * a, nt, ks, g, q, b0, b1);
+                mma_tf32(z[nt], xa[ks], b0, b1);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) z[nt][i] = -z[nt][i];
         }
-        uint32_t bx[4], fa[4];
-        c_to_b(acc, lane, bx);
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-        frag_a(Ym, 16 * a, 16 * a, 0, g, q, fa);
-        mma_tf32(y, fa, bx[0], bx[1]);
-        frag_a(Ym, 16 * a, 16 * a, 1, g, q, fa);
-        mma_tf32(y, fa, bx[2], bx[3]);
-        y[0] = -y[0]; y[1] = -y[1]; y[2] = -y[2]; y[3] = -y[3];   // Y_ab
-        const uint32_t col = 4u * q;   // byte offset of column n0 + 2q in its 16-byte chunk
-        *reinterpret_cast<uint32_t *>(x.sm + off_tb + swz(16 * a + g, n0 >> 3) + col) =
-            pack_bf16(y[0] * bt0, y[1] * bt1);
-        *reinterpret_cast<uint32_t *>(x.sm + off_tb + swz(16 * a + g + 8, n0 >> 3) + col) =
-            pack_bf16(y[2] * bt0, y[3] * bt1);
-        if (d < 3) c_to_b(y, lane, Bm[d]);
+        // T[16a + 8nt + 2q (+1)][16b + g (+8)] = Z[g (+8)][8nt + 2q (+1)] beta
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int t = 16 * a + 8 * nt + 2 * q;
+            uint8_t *tb = x.sm + off_tb;
+            *reinterpret_cast<__nv_bfloat16 *>(tb + swz(t, 2 * b) + 2 * g) = __float2bfloat16_rn(z[nt][0] * bt0);
+            *reinterpret_cast<__nv_bfloat16 *>(tb + swz(t + 1, 2 * b) + 2 * g) = __float2bfloat16_rn(z[nt][1] * bt0);
+            *reinterpret_cast<__nv_bfloat16 *>(tb + swz(t, 2 * b + 1) + 2 * g) = __float2bfloat16_rn(z[nt][2] * bt1);
+            *reinterpret_cast<__nv_bfloat16 *>(tb + swz(t + 1, 2 * b + 1) + 2 * g) = __float2bfloat16_rn(z[nt][3] * bt1);
+        }
+        if (d < 3) {
+            acc_to_a(z, za[d]);
+#pragma unroll
+            for (int d2 = d + 1; d2 <= 3; ++d2)
+                if (b + d2 <= 3) mma_zlt(acc[d2 - 1], za[d], Lm, b + d2, a, g, q);
+        }
     }
 }
 
-// Warps 6-7 (one row t each): the diagonal blocks T_aa = D_a Diag(beta) and the
+// Warps 3-4 (one row t each): the diagonal blocks T_aa = D_a Diag(beta) and the
 // zero blocks above the diagonal of the bf16 T tile.
 __device__ __forceinline__ void solve_diag_T(const Ctx &x, uint32_t off_tb) {
-    const int t = x.tid - 6 * 32;
+    const int t = x.tid - 3 * 32;
     const int a = t >> 4;
     float yr[16], bt[16];
     const float *src = x.Ym + t * LSTR + 16 * a;
@@ -513,12 +552,12 @@ __device__ __forceinline__ void phase_rhs_w8(const Ctx &x, uint32_t tm_ks, uint3
     for (int c4 = 0; c4 < 4; ++c4) st_chunk(x.sm + off_ru, swz(x.ch, 4 * half + c4), vt + 8 * c4);
 }
 
-// After the diagonal blocks: T (warps 0-7) and, in the fused kernel, RHS (warps 8-15).
+// After the diagonal blocks: T (warps 0-4) and, in the fused kernel, RHS (warps 8-15).
 __device__ __forceinline__ void solve_T(const Ctx &x, uint32_t off_tb, bool rhs, uint32_t tm_ks,
                                         uint32_t off_vt, uint32_t off_ru) {
-    if (x.warp < 6) solve_chain(x, off_tb);
-    else if (x.warp < 8) solve_diag_T(x, off_tb);
-    else if (rhs) phase_rhs_w8(x, tm_ks, off_vt, off_ru);
+    if (x.warp < 3) solve_chain(x, off_tb);
+    else if (x.warp < 5) solve_diag_T(x, off_tb);
+    else if (rhs && x.warp >= 8) phase_rhs_w8(x, tm_ks, off_vt, off_ru);
 }
 
 // ---- state-pass pieces shared by the fused and the state-only kernels ------
@@ -750,7 +789,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
             // =============================== phase A: gate, cumulative decay, operands
             if (tid < C) x.s_beta[tid] = beta_next;
-            phase_gate_operands(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
+            phase_gate_operands<false>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -771,16 +810,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             ++g_issued; ++s_issued;
             if (has_next) ++z_issued;
+            // while the MMAs run: V^T
+            if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
+            phase_vt(x, nvalid);
 
-            // =============================== phase B: P, L, V^T, T, RHS
+            // =============================== phase B: P, L, T, RHS
             if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
             if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, hx, (int)next_row, bar_qk);
             if (has_next) ++qk_issued;
-            if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
             phase_extract_PL(x, OFF_PB);
             __syncthreads();
-            phase_diag_and_vt(x, nvalid);
+            phase_diag(x);
             __syncthreads();
             if (tid == 0 && has_next) tma_2box(sm + OFF_V, &tm_v, hx, (int)next_row, bar_v);
             if (has_next) ++v_issued;
@@ -863,20 +904,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // ---- split path for batches with few chains ---------------------------------
 // With fewer (sequence, head) chains than about half the SMs, most of the GPU
 // would idle while each chain walks its chunks.  The state-independent work of
-// every chunk (gate, operands, Gram/P, the inverse) is then done first by
-// prefill_intra_kernel, over all chunks of a window in parallel, and exported
-// as one record per chunk; prefill_state_kernel (one CTA per chain) streams the
-// records with bulk copies and runs only the state-dependent MMAs.
+// every chunk is then done by prefill_intra_kernel, over all chunks of a window
+// in parallel: gate, operands, Gram/P, the inverse T, and W = T K~ and
+// U~ = T V on the tensor cores; it exports one record per chunk.
+// prefill_state_kernel (one CTA per chain) streams the records and runs the
+// state-dependent part in two MMA round trips per chunk:
+//   [U | Q~S0]^T = [U~ | 0]^T + S0^T [-W; Q~]^T,
+//   O^T = (Q~S0)^T + U^T P^T,   S1^T = S0^T Diag(e^{G_end}) + U^T Kend.
+// The host runs the state kernel of window k on the caller's stream while the
+// intra kernel of window k+1 runs on a side stream (records double-buffered,
+// ordered by events only).
 
 // Exported record of one chunk (bf16 operand tiles in their smem layout).
-constexpr uint32_t REC_B1 = 0;         // [K~; Q~] 128 x 128
+constexpr uint32_t REC_B1 = 0;         // [-W; Q~] 128 x 128
 constexpr uint32_t REC_KE = 32768;     // Kend^T [c][s] 128 x 64
-constexpr uint32_t REC_TB = 49152;     // T [t][s] 64 x 64
-constexpr uint32_t REC_PB = 57344;     // P [t][s] 64 x 64
-constexpr uint32_t REC_VT = 65536;     // V^T [j][s] 128 x 64 (rows past the end zeroed)
-constexpr uint32_t REC_G = 81920;      // 2^(G_end), 128 float
-constexpr uint32_t REC_BYTES = 82432;
+constexpr uint32_t REC_PB = 49152;     // P [t][s] 64 x 64
+constexpr uint32_t REC_UT = 57344;     // U~^T [j][t] 128 x 64
+constexpr uint32_t REC_G = 73728;      // 2^(G_end), 128 float
+constexpr uint32_t REC_BYTES = 74240;
 constexpr uint32_t OFF_TB_INTRA = OFF_ST;   // the intra kernel keeps T where the state tile would be
+constexpr uint32_t OFF_UT_INTRA = OFF_GB;   // U~^T staging, over the solve scratch once T is done
+constexpr uint32_t TM_W = 0, TM_UT = 64;    // intra kernel: W^T and U~^T accumulators (N = 64)
+static_assert(OFF_KT + 16384 <= OFF_MISC, "K~^T tile overlaps");
+static_assert(OFF_UT_INTRA + 16384 <= OFF_B1, "U~^T staging overlaps");
 
 struct SplitParams {
     const float *A;
@@ -936,6 +986,23 @@ __device__ __forceinline__ bool item_info(const SplitParams &p, int it, ItemInfo
     return true;
 }
 
+// W^T and U~^T out of TMEM: -W into rows 0..63 of the [-W; Q~] tile (over K~,
+// which the record does not need), U~^T into its staging tile.
+__device__ __forceinline__ void phase_wu_out(const Ctx &x) {
+    float Wt[16], Ut[16];
+    ptx::tmem_ld16(x.lane_base + TM_W + 16 * x.cg, Wt);    // W^T[c][16 cg + i], c = ch
+    ptx::tmem_ld16(x.lane_base + TM_UT + 16 * x.cg, Ut);   // U~^T[j][16 cg + i], j = ch
+    ptx::tmem_ld_wait();
+    const int c = x.ch;
+    uint8_t *b1 = x.sm + OFF_B1 + (c >> 6) * 16384;
+    const uint32_t cc = (uint32_t)((c & 63) >> 3), ci = (uint32_t)(c & 7) * 2u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<__nv_bfloat16 *>(b1 + swz(16 * x.cg + i, cc) + ci) = __float2bfloat16_rn(-Wt[i]);
+    st_chunk(x.sm + OFF_UT_INTRA, swz(c, 2 * x.cg), Ut);
+    st_chunk(x.sm + OFF_UT_INTRA, swz(c, 2 * x.cg + 1), Ut + 8);
+}
+
 __global__ void __launch_bounds__(NT, 1)
 prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -947,7 +1014,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint64_t *bar_qk = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *bar_z = bar_qk + 1;
     uint64_t *bar_v = bar_qk + 2;
-    uint64_t *bar_g = bar_qk + 3;
+    uint64_t *bar_g = bar_qk + 3;      // Gram/P MMA, then W/U~ MMAs done
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + OFF_SLOT);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 8);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -992,7 +1059,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         int nit = it + gridDim.x;
         while (nit < n_items && !item_info(p, nit, nxt)) nit += gridDim.x;
         const bool has_next = nit < n_items;
-        const int hx = cur.h * D, nhx = has_next ? nxt.h * D : 0;
+        const int nhx = has_next ? nxt.h * D : 0;
         const int nvalid = cur.nvalid;
         uint8_t *rec = p.records + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * REC_BYTES;
 
@@ -1001,7 +1068,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (tid == 0) ptx::bulk_wait_read();   // the previous item's exports have left smem
         __syncthreads();
 
-        phase_gate_operands(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
+        phase_gate_operands<true>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
@@ -1012,28 +1079,27 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             mma_k<8>(tmem + TM_G, sbase + OFF_QK, 16384u, sbase + OFF_GB, GB_KBLK,
                      ptx::idesc_bf16_f32(128, 160), false);
             ptx::mma_commit(bar_g);
-            bulk_store(rec + REC_B1, sm + OFF_B1, 32768);
             bulk_store(rec + REC_KE, sm + OFF_KE, 16384);
             bulk_store(rec + REC_G, reinterpret_cast<const uint8_t *>(x.s_gamma), 512);
             ptx::bulk_commit();
         }
         ++g_issued;
         if (has_next) ++z_issued;
+        if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
+        phase_vt(x, nvalid);
 
         if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
         if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, nhx, (int)nxt.row0, bar_qk);
         if (has_next) ++qk_issued;
-        if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
         phase_extract_PL(x, OFF_PB);
-        __syncthreads();
-        phase_diag_and_vt(x, nvalid);
         ptx::fence_async_smem();
+        __syncthreads();
+        phase_diag(x);
         __syncthreads();
         if (tid == 0) {
             if (has_next) tma_2box(sm + OFF_V, &tm_v, nhx, (int)nxt.row0, bar_v);
             bulk_store(rec + REC_PB, sm + OFF_PB, 8192);
-            bulk_store(rec + REC_VT, sm + OFF_VT, 16384);
             ptx::bulk_commit();
         }
         if (has_next) ++v_issued;
@@ -1043,7 +1109,25 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __syncthreads();
         if (*s_abort) break;
         if (tid == 0) {
-            bulk_store(rec + REC_TB, sm + OFF_TB_INTRA, 8192);
+            ptx::tc_fence_after_sync();
+            // W^T[c][t] = K~^T[c] . T[t] and U~^T[j][t] = V^T[j] . T[t]
+            mma_k<4>(tmem + TM_W, sbase + OFF_KT, 0u, sbase + OFF_TB_INTRA, 0u,
+                     ptx::idesc_bf16_f32(128, 64), false);
+            mma_k<4>(tmem + TM_UT, sbase + OFF_VT, 0u, sbase + OFF_TB_INTRA, 0u,
+                     ptx::idesc_bf16_f32(128, 64), false);
+            ptx::mma_commit(bar_g);
+        }
+        ++g_issued;
+        if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
+        ptx::tc_fence_after_sync();
+        phase_wu_out(x);
+        ptx::fence_async_smem();
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        if (*s_abort) break;
+        if (tid == 0) {
+            bulk_store(rec + REC_B1, sm + OFF_B1, 32768);
+            bulk_store(rec + REC_UT, sm + OFF_UT_INTRA, 16384);
             ptx::bulk_commit();
         }
         it = nit;
@@ -1068,14 +1152,29 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 }
 
 // ---- state-only kernel: shared memory map ------------------------------------
-constexpr uint32_t SB_STAGE = 83968;            // record stage stride (1024-aligned)
-constexpr uint32_t SB_ST = 2 * SB_STAGE - 1024; // 166912: S^T bf16 (after stage 1's 82432 bytes)
-constexpr uint32_t SB_RU = SB_ST + 32768;       // RHS^T / U^T, then the output tile
+constexpr uint32_t SB_STAGE = 74752;            // record stage stride (1024-aligned)
+constexpr uint32_t SB_ST = 2 * SB_STAGE;        // S^T bf16 (A of the first MMA)
+constexpr uint32_t SB_RU = SB_ST + 32768;       // U^T, then the output tile
 constexpr uint32_t SB_BAR = SB_RU + 16384;      // mbarriers and slots
 constexpr uint32_t SMEM_STATE = SB_BAR + 128 + 1024;
-static_assert(SB_STAGE + REC_BYTES <= SB_ST, "stages overlap the state tile");
+static_assert(REC_BYTES <= SB_STAGE && SB_STAGE % 1024 == 0, "record stage");
 static_assert(SMEM_STATE <= 232448, "shared memory budget");
-constexpr uint32_t TS_D1 = 0, TS_D2 = 128, TS_D3 = 256;   // TMEM columns
+constexpr uint32_t TS_D1 = 0;     // two buffers of 128 columns: [U^T | (Q~S0 + PU)^T]
+constexpr uint32_t TS_D3 = 256;   // float32 master S^T
+
+// [U~^T | 0] of a chunk into a D1 buffer: column groups 0-1 copy U~^T, 2-3 zero.
+__device__ __forceinline__ void preload_u(const Ctx &x, uint32_t tm_d1, const uint8_t *ut) {
+    float v[32];
+    if (x.cg < 2) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) ld_chunk(ut, swz(x.ch, 4 * x.cg + c4), v + 8 * c4);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    }
+    ptx::tmem_st32(x.lane_base + tm_d1 + 32 * x.cg, v);
+    ptx::tmem_st_wait();
+}
 
 __global__ void __launch_bounds__(NT, 1)
 prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams p) {
@@ -1131,22 +1230,27 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         if (c0 + k < c_end) ++st_issued[k];
     const float *src = first ? (p.initial_state ? p.initial_state + sidx : nullptr) : p.states + sidx;
     load_state(x, src, TS_D3, SB_ST);
+    if (c0 < c_end) {
+        if (ptx::mbar_wait(bar_st, st_done[0] & 1, kWaitBudget)) ++st_done[0]; else *s_abort = 1;
+        preload_u(x, TS_D1, sm + REC_UT);
+    }
     ptx::fence_async_smem();
     ptx::tc_fence_before_sync();
     __syncthreads();
 
     for (int c = c0; c < c_end; ++c) {
+        if (*s_abort) break;
         const int k = (c - c0) & 1;
         uint8_t *stg = sm + k * SB_STAGE;
         const uint32_t sstg = sbase + k * SB_STAGE;
+        const uint32_t d1 = TS_D1 + 128 * k;
         const int64_t row0 = bos + (int64_t)c * C;
         const int nvalid = (int)((eos - row0) < C ? (eos - row0) : C);
-        if (ptx::mbar_wait(bar_st + k, st_done[k] & 1, kWaitBudget)) ++st_done[k]; else *s_abort = 1;
         if (tid == 0) {
             ptx::tc_fence_after_sync();
-            // D1[j][s|t] = S^T[j] . [K~;Q~][s|t]
-            mma_k<8>(tmem + TS_D1, sbase + SB_ST, 16384u, sstg + REC_B1, 16384u,
-                     ptx::idesc_bf16_f32(128, 128), false);
+            // D1 = [U~ | 0]^T + S^T [-W; Q~]^T
+            mma_k<8>(tmem + d1, sbase + SB_ST, 16384u, sstg + REC_B1, 16384u,
+                     ptx::idesc_bf16_f32(128, 128), true);
             ptx::mma_commit(bar_s);
             ptx::bulk_wait_read();   // the previous output tile has left RU
         }
@@ -1154,40 +1258,34 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         __syncthreads();
         if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
-        phase_rhs(x, TS_D1, REC_VT + k * SB_STAGE, SB_RU);
+        phase_u_scale(x, d1, TS_D3, SB_RU, reinterpret_cast<const float *>(stg + REC_G));
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
         if (*s_abort) break;
         if (tid == 0) {
             ptx::tc_fence_after_sync();
-            mma_k<4>(tmem + TS_D2, sbase + SB_RU, 0u, sstg + REC_TB, 0u, ptx::idesc_bf16_f32(128, 64), false);
-            ptx::mma_commit(bar_m);
-        }
-        ++m_issued;
-        if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
-        ptx::tc_fence_after_sync();
-        phase_u_scale(x, TS_D2, TS_D3, SB_RU, reinterpret_cast<const float *>(stg + REC_G));
-        ptx::fence_async_smem();
-        ptx::tc_fence_before_sync();
-        __syncthreads();
-        if (*s_abort) break;
-        if (tid == 0) {
-            ptx::tc_fence_after_sync();
-            mma_k<4>(tmem + TS_D1 + 64, sbase + SB_RU, 0u, sstg + REC_PB, 0u, ptx::idesc_bf16_f32(128, 64), true);
+            // O^T += U^T P^T ; S^T += U^T Kend
+            mma_k<4>(tmem + d1 + 64, sbase + SB_RU, 0u, sstg + REC_PB, 0u, ptx::idesc_bf16_f32(128, 64), true);
             mma_k<4>(tmem + TS_D3, sbase + SB_RU, 0u, sstg + REC_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
             ptx::mma_commit(bar_m);
         }
         ++m_issued;
+        // meanwhile: the next chunk's [U~ | 0] into the other D1 buffer
+        if (c + 1 < c_end) {
+            if (ptx::mbar_wait(bar_st + (k ^ 1), st_done[k ^ 1] & 1, kWaitBudget)) ++st_done[k ^ 1];
+            else *s_abort = 1;
+            preload_u(x, TS_D1 + 128 * (k ^ 1), sm + (k ^ 1) * SB_STAGE + REC_UT);
+        }
         if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
-        phase_state_out(x, TS_D3, TS_D1 + 64, SB_ST, SB_RU);
+        phase_state_out(x, TS_D3, d1 + 64, SB_ST, SB_RU);
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
         if (*s_abort) break;
         store_output(x, &tm_o, SB_RU, p.out, row0, nvalid, hx, rowstride);
-        // this stage has been consumed: fetch the record two chunks ahead into it
+        // stage k has been consumed: fetch the record two chunks ahead into it
         if (tid == 0 && c + 2 < c_end)
             bulk_load(stg, recs + (size_t)(c + 2 - c0) * REC_BYTES, REC_BYTES, bar_st + k);
         if (c + 2 < c_end) ++st_issued[k];
@@ -1262,15 +1360,17 @@ static int sm_count() {
 }
 
 // Split-path plan: used when the chains fill at most half the SMs and the
-// sequences average at least 8 chunks.  Workspace after the schedule area:
-// the carried states, then W record slots per chain.
+// sequences average at least 8 chunks.  The chunks are taken in windows of W
+// per chain; workspace after the schedule area: the states carried between
+// windows, then two record buffers of W slots per chain (window k uses buffer
+// k % 2, so the intra kernel of window k + 1 can run beside the state kernel of
+// window k).
 struct SplitPlan {
     bool ok;
-    int W;
+    int W, windows;
     int64_t max_chunks;
-    size_t states_off, records_off, bytes;
+    size_t states_off, records_off, window_bytes, bytes;
 };
-constexpr int kSplitWindow = 256;
 
 static SplitPlan plan_split(int64_t total, int num_seqs, int H) {
     SplitPlan s{};
@@ -1278,11 +1378,15 @@ static SplitPlan plan_split(int64_t total, int num_seqs, int H) {
     s.max_chunks = (total + tc::C - 1) / tc::C;
     s.ok = chains > 0 && 2 * chains <= sm_count() && total >= (int64_t)8 * tc::C * num_seqs;
     if (!s.ok) return s;
-    s.W = (int)(s.max_chunks < kSplitWindow ? s.max_chunks : kSplitWindow);
+    int64_t W = (s.max_chunks + 3) / 4;   // about four windows, 8..256 chunks each
+    W = W < 8 ? 8 : (W > 256 ? 256 : W);
+    s.W = (int)W;
+    s.windows = (int)((s.max_chunks + W - 1) / W);
     const size_t base = (kWsOrder + sizeof(int32_t) * (size_t)num_seqs + 1023) & ~size_t(1023);
     s.states_off = base;
     s.records_off = base + (size_t)chains * tc::D * tc::D * sizeof(float);
-    s.bytes = s.records_off + (size_t)chains * s.W * tc::REC_BYTES;
+    s.window_bytes = (size_t)chains * s.W * tc::REC_BYTES;
+    s.bytes = s.records_off + 2 * s.window_bytes;
     return s;
 }
 
@@ -1291,6 +1395,36 @@ static SplitPlan plan_split(int64_t total, int num_seqs, int H) {
 size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H) {
     const SplitPlan s = plan_split(total, num_seqs, H);
     return s.ok ? s.bytes : 0;
+}
+
+// The split plan's side stream and events, one set per device, created on
+// first use and kept until the process exits.  The mutex also keeps the
+// event bookkeeping of calls from several host threads apart.
+struct SideStream {
+    cudaStream_t s;
+    cudaEvent_t fork, intra[2], state[2];
+};
+constexpr int kMaxDevices = 64;
+static std::mutex g_side_mu;
+static SideStream g_side[kMaxDevices];
+
+static cudaError_t side_stream(SideStream **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideStream &ss = g_side[dev];
+    if (!ss.s) {
+        SideStream n{};
+        e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
+        cudaEvent_t *evs[5] = {&n.fork, &n.intra[0], &n.intra[1], &n.state[0], &n.state[1]};
+        for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+            e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        ss = n;
+    }
+    *out = &ss;
+    return cudaSuccess;
 }
 
 cudaError_t launch_schedule(const int32_t *cu, int num_seqs, int32_t *order, uint32_t *counter,
@@ -1322,20 +1456,37 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         e = cudaFuncSetAttribute(tc::prefill_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)tc::SMEM_STATE);
         if (e != cudaSuccess) return e;
+        std::lock_guard<std::mutex> lock(g_side_mu);
+        SideStream *ss = nullptr;
+        e = side_stream(&ss);
+        if (e != cudaSuccess) return e;
         tc::SplitParams sp;
         sp.A = A; sp.beta = beta; sp.cu_seqlens = cu; sp.initial_state = s0; sp.final_state = s1;
         sp.out = static_cast<__nv_bfloat16 *>(out);
-        sp.records = ws + plan.records_off;
         sp.states = reinterpret_cast<float *>(ws + plan.states_off);
         sp.status = status; sp.total_tokens = total; sp.num_seqs = num_seqs; sp.H = H;
         sp.W = plan.W;
-        for (int64_t w0 = 0; w0 < plan.max_chunks; w0 += plan.W) {
+        // fork: the side stream starts after everything already on `st`
+        if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
+        for (int wi = 0; wi < plan.windows; ++wi) {
+            const int buf = wi & 1;
+            const int64_t w0 = (int64_t)wi * plan.W;
             sp.w0 = (int)w0;
             sp.wn = (int)((plan.max_chunks - w0) < plan.W ? (plan.max_chunks - w0) : plan.W);
+            sp.records = ws + plan.records_off + buf * plan.window_bytes;
+            // buffer `buf` was last read by the state kernel of window wi - 2
+            if (wi >= 2 && (e = cudaStreamWaitEvent(ss->s, ss->state[buf], 0)) != cudaSuccess) return e;
             const int64_t items = chains * sp.wn;
-            const int grid = (int)(items < sms ? items : sms);
-            tc::prefill_intra_kernel<<<grid, tc::NT, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mz, sp);
+            const int64_t cap = wi == 0 ? sms : sms - chains;   // leave room for the state kernel
+            const int grid = (int)(items < cap ? items : cap);
+            tc::prefill_intra_kernel<<<grid, tc::NT, tc::SMEM_ALLOC, ss->s>>>(mq, mk, mv, mz, sp);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if ((e = cudaEventRecord(ss->intra[buf], ss->s)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(st, ss->intra[buf], 0)) != cudaSuccess) return e;
             tc::prefill_state_kernel<<<(unsigned)chains, tc::NT, tc::SMEM_STATE, st>>>(mo, sp);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if ((e = cudaEventRecord(ss->state[buf], st)) != cudaSuccess) return e;
         }
         return cudaGetLastError();
     }
