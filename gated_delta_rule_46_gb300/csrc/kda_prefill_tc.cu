@@ -923,10 +923,11 @@ constexpr uint32_t REC_UT = 57344;     // U~^T [j][t] 128 x 64
 constexpr uint32_t REC_G = 73728;      // 2^(G_end), 128 float
 constexpr uint32_t REC_BYTES = 74240;
 constexpr uint32_t OFF_TB_INTRA = OFF_ST;   // the intra kernel keeps T where the state tile would be
-constexpr uint32_t OFF_UT_INTRA = OFF_GB;   // U~^T staging, over the solve scratch once T is done
+constexpr uint32_t OFF_UT_INTRA = OFF_PB;   // U~^T staging: P (exported by then) and the unused 8 KB after it
+constexpr uint32_t OFF_NW_INTRA = OFF_VT;   // -W staging (two 64-row K-block halves), over V^T once the MMAs ran
 constexpr uint32_t TM_W = 0, TM_UT = 64;    // intra kernel: W^T and U~^T accumulators (N = 64)
 static_assert(OFF_KT + 16384 <= OFF_MISC, "K~^T tile overlaps");
-static_assert(OFF_UT_INTRA + 16384 <= OFF_B1, "U~^T staging overlaps");
+static_assert(OFF_UT_INTRA + 16384 <= OFF_GB && OFF_NW_INTRA + 16384 <= OFF_PB, "staging overlaps");
 
 struct SplitParams {
     const float *A;
@@ -986,15 +987,15 @@ __device__ __forceinline__ bool item_info(const SplitParams &p, int it, ItemInfo
     return true;
 }
 
-// W^T and U~^T out of TMEM: -W into rows 0..63 of the [-W; Q~] tile (over K~,
-// which the record does not need), U~^T into its staging tile.
+// W^T and U~^T out of TMEM into their staging tiles: -W as the two 64-row
+// K-block halves of the [-W; Q~] operand, U~^T [j][t].
 __device__ __forceinline__ void phase_wu_out(const Ctx &x) {
     float Wt[16], Ut[16];
     ptx::tmem_ld16(x.lane_base + TM_W + 16 * x.cg, Wt);    // W^T[c][16 cg + i], c = ch
     ptx::tmem_ld16(x.lane_base + TM_UT + 16 * x.cg, Ut);   // U~^T[j][16 cg + i], j = ch
     ptx::tmem_ld_wait();
     const int c = x.ch;
-    uint8_t *b1 = x.sm + OFF_B1 + (c >> 6) * 16384;
+    uint8_t *b1 = x.sm + OFF_NW_INTRA + (c >> 6) * 8192;
     const uint32_t cc = (uint32_t)((c & 63) >> 3), ci = (uint32_t)(c & 7) * 2u;
 #pragma unroll
     for (int i = 0; i < 16; ++i)
@@ -1046,7 +1047,10 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     ItemInfo cur, nxt;
     int it = blockIdx.x;
     while (it < n_items && !item_info(p, it, cur)) it += gridDim.x;
+    float ean_cur = 0.f, beta_cur = 0.f;   // this thread's entry of s_eAn / s_beta for the coming item
     if (it < n_items) {
+        if (tid < D) ean_cur = -expf(p.A[cur.h * D + tid]) * kLog2e;
+        if (tid < C) beta_cur = (tid < cur.nvalid) ? p.beta[(cur.row0 + tid) * H + cur.h] : 0.f;
         if (tid == 0) {
             const int hx = cur.h * D;
             tma_qk(sm, &tm_q, &tm_k, hx, (int)cur.row0, bar_qk);
@@ -1063,12 +1067,19 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int nvalid = cur.nvalid;
         uint8_t *rec = p.records + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * REC_BYTES;
 
-        if (tid < D) x.s_eAn[tid] = -expf(p.A[cur.h * D + tid]) * kLog2e;
-        if (tid < C) x.s_beta[tid] = (tid < nvalid) ? p.beta[(cur.row0 + tid) * H + cur.h] : 0.f;
-        if (tid == 0) ptx::bulk_wait_read();   // the previous item's exports have left smem
+        if (tid < D) x.s_eAn[tid] = ean_cur;
+        if (tid < C) x.s_beta[tid] = beta_cur;
+        // every export but the previous item's last group (-W, U~^T) has left smem
+        if (tid == 0) ptx::bulk_wait_read_but1();
         __syncthreads();
+        // the next item's gate constants and beta, loaded while this one runs
+        if (has_next) {
+            if (tid < D) ean_cur = -expf(p.A[nxt.h * D + tid]) * kLog2e;
+            if (tid < C) beta_cur = (tid < nxt.nvalid) ? p.beta[(nxt.row0 + tid) * H + nxt.h] : 0.f;
+        }
 
         phase_gate_operands<true>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
+        if (tid == 0) ptx::bulk_wait_read();   // -W and U~^T staging free for this item
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
@@ -1081,6 +1092,8 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             ptx::mma_commit(bar_g);
             bulk_store(rec + REC_KE, sm + OFF_KE, 16384);
             bulk_store(rec + REC_G, reinterpret_cast<const uint8_t *>(x.s_gamma), 512);
+            bulk_store(rec + REC_B1 + 8192, sm + OFF_B1 + 8192, 8192);                 // Q~, K-block 0
+            bulk_store(rec + REC_B1 + 16384 + 8192, sm + OFF_B1 + 16384 + 8192, 8192); // Q~, K-block 1
             ptx::bulk_commit();
         }
         ++g_issued;
@@ -1110,6 +1123,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (*s_abort) break;
         if (tid == 0) {
             ptx::tc_fence_after_sync();
+            ptx::bulk_wait_read();   // P has left its tile (U~^T staging goes there)
             // W^T[c][t] = K~^T[c] . T[t] and U~^T[j][t] = V^T[j] . T[t]
             mma_k<4>(tmem + TM_W, sbase + OFF_KT, 0u, sbase + OFF_TB_INTRA, 0u,
                      ptx::idesc_bf16_f32(128, 64), false);
@@ -1126,7 +1140,8 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __syncthreads();
         if (*s_abort) break;
         if (tid == 0) {
-            bulk_store(rec + REC_B1, sm + OFF_B1, 32768);
+            bulk_store(rec + REC_B1, sm + OFF_NW_INTRA, 8192);                  // -W, K-block 0
+            bulk_store(rec + REC_B1 + 16384, sm + OFF_NW_INTRA + 8192, 8192);   // -W, K-block 1
             bulk_store(rec + REC_UT, sm + OFF_UT_INTRA, 16384);
             ptx::bulk_commit();
         }
@@ -1163,8 +1178,16 @@ constexpr uint32_t TS_D1 = 0;     // two buffers of 128 columns: [U^T | (Q~S0 + 
 constexpr uint32_t TS_D3 = 256;   // float32 master S^T
 
 // [U~^T | 0] of a chunk into a D1 buffer: column groups 0-1 copy U~^T, 2-3 zero.
+// Warp 0 is busy issuing MMAs when this runs, so warp 8 (the same TMEM lane
+// quarter) also takes its share.
 __device__ __forceinline__ void preload_u(const Ctx &x, uint32_t tm_d1, const uint8_t *ut) {
+    if (x.warp == 0) return;
     float v[32];
+    if (x.warp == 8) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) ld_chunk(ut, swz(x.ch, c4), v + 8 * c4);
+        ptx::tmem_st32(x.lane_base + tm_d1, v);
+    }
     if (x.cg < 2) {
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) ld_chunk(ut, swz(x.ch, 4 * x.cg + c4), v + 8 * c4);
