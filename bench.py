@@ -218,6 +218,7 @@ def run_gpu(args):
     out1 = torch.empty((T1, H1, 128), dtype=torch.bfloat16, device=dev)
     fin1 = torch.empty((1, H1, 128, 128), dtype=torch.float32, device=dev)
     ws1 = torch.zeros(kda.workspace_size(T1, 1, H1, 128, 128), dtype=torch.uint8, device=dev)
+    L_pref = kda.prefill_kernel_launches(T1, 1, H1, 128, 128, torch.bfloat16, ws1.numel())
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MB > L2
 
     # ---- decode workload: 128 steps of inputs pre-generated on the device
@@ -338,9 +339,9 @@ def run_gpu(args):
                 "traffic": _ncu_traffic("decode_kernel", "kda_simt.cu"),
                 "algorithmic_bytes_per_launch": alg_dec, "peak_source": peak_kind,
                 "us_per_launch": per_launch_dec * 1e6}
-    roof_pref = {"kernel": "kda_chunk_prefill (schedule + intra-chunk + state-pass kernels)", "bound": "hbm",
+    roof_pref = {"kernel": f"kda_chunk_prefill ({L_pref} launches: schedule, then intra-chunk and state-pass kernel per window)", "bound": "hbm",
                  "achieved": ach_pref, "peak": peak, "unit": "GB/s", "frac": ach_pref / peak,
-                 "traffic": _ncu_traffic("prefill_tc_kernel", "kda_prefill_tc.cu"),
+                 "traffic": _ncu_traffic("kda_chunk_prefill_T4096_H16", "kda_prefill_tc.cu"),
                  "algorithmic_bytes_per_launch": alg_pref, "peak_source": peak_kind,
                  "us_per_launch": per_launch_pref * 1e6}
 
@@ -380,7 +381,7 @@ def run_gpu(args):
                     "h2d_bytes_per_step": h2d_pref + h2d_dec, "d2h_bytes_per_step": d2h_pref + d2h_dec,
                     "decode_value": dec_tokens / e2d},
             "prefill_large": extra,
-            "gpu_launches": K * (3 + NS),
+            "gpu_launches": K * (L_pref + NS),
             "clocks": clk.result,
             "device_status": ok_status,
             "cpu_baseline": cpu,
@@ -392,15 +393,28 @@ def run_gpu(args):
     return 0
 
 
+# Prefill cases timed on their own (`--case`), e.g. as the command an ncu
+# capture runs: (name, workload id or sequence lengths, H).
+CASES = {
+    "prefill": ("prefill", 1, None),
+    "varlen": ("varlen", 2, None),
+    "long": ("long", 3, None),
+    # the fused (many-chain) plan at a size an ncu capture can replay: 1.4 GB
+    "fused-16x2048": ("fused-16x2048: 16 seqs x 2048 tokens", [2048] * 16, 32),
+}
+
+
 def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, peak, peak_kind,
-                        reps=2):
-    """One KDA layer over the varlen (64 packed sequences) or the 1M-token
-    workload: inputs drawn on the device with the same distributions as the
-    parity inputs (bf16 q/k L2-normalised, v/z N(0,1), beta = sigmoid(N(0,1)),
+                        reps=2, warm=1, lens=None, H=None, name=None):
+    """One KDA layer over a packed batch (by default the varlen or the 1M-token
+    workload `wid`): inputs drawn on the device with the same distributions as
+    the parity inputs (bf16 q/k L2-normalised, v/z N(0,1), beta = sigmoid(N(0,1)),
     A ~ U(-1,1), zero initial state), outputs and final states written."""
     import torch
-    w = inputs.workload(wid)
-    T, H, d = w.total_tokens, w.H, w.dk
+    if lens is None:
+        w = inputs.workload(wid)
+        lens, H, name = list(w.seq_lens), w.H, w.name
+    T, d = sum(lens), 128
     g = torch.Generator(device=dev)
     g.manual_seed(1000 + 7 * wid + seed)
 
@@ -413,9 +427,9 @@ def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, pe
     z = normal((T, H, d)).to(torch.bfloat16)
     beta = torch.sigmoid(normal((T, H)))
     A = torch.rand((H, d), generator=g, device=dev) * 2 - 1
-    cu = torch.zeros(len(w.seq_lens) + 1, dtype=torch.int32, device=dev)
-    cu[1:] = torch.cumsum(torch.tensor(w.seq_lens, device=dev), 0)
-    N = len(w.seq_lens)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32, device=dev)
+    cu[1:] = torch.cumsum(torch.tensor(lens, device=dev), 0)
+    N = len(lens)
     out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
     fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
     ws = torch.zeros(kda.workspace_size(T, N, H, d, d), dtype=torch.uint8, device=dev)
@@ -424,7 +438,8 @@ def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, pe
     def call():
         kda.chunk_prefill(q, k, v, z, A, beta, cu, None, final_state=fin, out=out, workspace=ws)
 
-    call()
+    for _ in range(warm):
+        call()
     barrier()
     times = []
     for _ in range(reps):
@@ -441,7 +456,7 @@ def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, pe
     status = kda.check_device_status(ws)
     del q, k, v, z, out, ws
     torch.cuda.empty_cache()
-    return {"workload": f"{w.name}: {N} seqs, {T} tokens, H={H}, dk=dv={d}, bf16, zero state",
+    return {"workload": f"{name}: {N} seqs, {T} tokens, H={H}, dk=dv={d}, bf16, zero state",
             "value": T / t, "unit": "tokens/s", "ms_per_call": 1000 * t,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                          "frac": ach / peak, "algorithmic_bytes_per_launch": alg,
@@ -458,12 +473,36 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra-workloads", action="store_true",
                     help="skip the varlen and 1M-token prefill measurements")
+    ap.add_argument("--case", choices=sorted(CASES),
+                    help="time one prefill case alone (--warmup untimed, --steps timed calls) "
+                         "and print its JSON line; no decode, no CPU baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
     return run_gpu(args)
+
+
+def run_case(args):
+    import torch
+    import gated_delta_rule_46_gb300 as kda
+    from gated_delta_rule_46_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    kda.lib()
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MB > L2
+    name, spec, H = CASES[args.case]
+    peak, peak_kind = _peaks()
+    kw = {} if isinstance(spec, int) else {"lens": spec, "H": H, "name": name}
+    wid = spec if isinstance(spec, int) else 77
+    r = _time_large_prefill(kda, inputs, wid, dev, 0, flush, torch.cuda.synchronize,
+                            lambda x: x, peak, peak_kind, reps=args.steps, warm=args.warmup, **kw)
+    r.update({"case": args.case, "steps": args.steps, "warmup": args.warmup,
+              "l2": "flushed before every timed call (256 MB write)"})
+    print(json.dumps(r))
+    return 0
 
 
 if __name__ == "__main__":

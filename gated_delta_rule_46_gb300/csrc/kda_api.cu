@@ -23,6 +23,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
                               void *out, void *workspace, size_t workspace_bytes, cudaStream_t st);
 size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H);
+int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes);
 }  // namespace kda
 
 namespace {
@@ -81,6 +82,15 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int
         if (extra > bytes) bytes = (extra + 255) & ~size_t(255);
     }
     return bytes;
+}
+
+int kda_prefill_kernel_launches(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                kda_dtype_t dtype, size_t workspace_bytes) {
+    if (num_seqs <= 0 || H <= 0) return 0;
+    if (dtype == KDA_BF16 && dk == 128 && dv == 128 && total_tokens > 0 &&
+        total_tokens < (int64_t(1) << 31))
+        return kda::prefill_tc_launches(total_tokens, num_seqs, H, workspace_bytes);
+    return 1;
 }
 
 kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,

@@ -1420,6 +1420,13 @@ size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H) {
     return s.ok ? s.bytes : 0;
 }
 
+// Kernels one tensor-core prefill launches: the schedule kernel, then either
+// the fused kernel or an intra and a state kernel per window.
+int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes) {
+    const SplitPlan s = plan_split(total, num_seqs, H);
+    return 1 + ((s.ok && workspace_bytes >= s.bytes) ? 2 * s.windows : 1);
+}
+
 // The split plan's side stream and events, one set per device, created on
 // first use and kept until the process exits.  The mutex also keeps the
 // event bookkeeping of calls from several host threads apart.

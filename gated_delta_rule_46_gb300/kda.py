@@ -54,6 +54,8 @@ def lib():
             L.kda_chunk_prefill.restype = I
             L.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P]
             L.kda_decode_step.restype = I
+            L.kda_prefill_kernel_launches.argtypes = [I64, I, I, I, I, I, SZ]
+            L.kda_prefill_kernel_launches.restype = I
             L.kda_check_device_status.argtypes = [P, P]
             L.kda_check_device_status.restype = I
             _lib = L
@@ -154,6 +156,13 @@ def chunk_prefill(q, k, v, z, A, beta, cu_seqlens, initial_state=None, final_sta
                                  _ptr(workspace), workspace.numel(), _stream(stream))
     _raise(st, "kda_chunk_prefill")
     return out, final_state
+
+
+def prefill_kernel_launches(total_tokens, num_seqs, H, dk, dv, dtype, workspace_bytes) -> int:
+    """Kernels one chunk_prefill call with these sizes launches (see the C header)."""
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib().kda_prefill_kernel_launches(total_tokens, num_seqs, H, dk, dv, code,
+                                                 workspace_bytes))
 
 
 def check_device_status(workspace: torch.Tensor, stream=None) -> int:

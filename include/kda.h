@@ -82,9 +82,9 @@ kda_status_t kda_gate(const void *z, kda_dtype_t z_dtype, const float *A, float 
  * accepts is 256 + 4 * num_seqs bytes (rounded up to 256): a status word, a
  * work counter and a schedule.  For bf16, dk = dv = 128 batches with few
  * (sequence, head) chains (at most half the SM count) the returned size also
- * holds the chunk-parallel plan's per-chunk records (about 80 KB per chunk of
- * a window of at most 256 chunks per chain) and one carried state per chain;
- * with less than that the call falls back to the one-kernel plan.  The
+ * holds the chunk-parallel plan's per-chunk records (72.5 KB per chunk, two
+ * buffers of a window of 8 to 256 chunks per chain) and one carried state per
+ * chain; with less than that the call falls back to the one-kernel plan.  The
  * workspace holds no data between calls except the status word, which every
  * call clears on entry.
  */
@@ -110,9 +110,13 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int
  * Length-0 sequences copy their initial state (or zeros) to final_state.
  * bf16 inputs with dk = dv = 128 run the chunkwise tensor-core path (64-token
  * chunks, 16-token decay tiles): one persistent kernel over the chains when
- * they fill the GPU, else a chunk-parallel kernel for the state-independent
- * work followed by a per-chain state-pass kernel.  Every other supported case
- * runs the token-serial float32 kernel.
+ * they fill the GPU, else, window by window, a chunk-parallel kernel for the
+ * state-independent work and a per-chain state-pass kernel.  That split plan
+ * runs the chunk-parallel kernel of the next window on an internal stream
+ * (one per device, created on the first such call and kept until exit,
+ * joined back to `stream` with events), so the call stays ordered on
+ * `stream` as a whole; calls from several host threads take turns on it.
+ * Every other supported case runs the token-serial float32 kernel.
  */
 kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,
                                const float *A, const float *beta, const int32_t *cu_seqlens,
@@ -120,6 +124,16 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
                                kda_dtype_t dtype, const float *initial_state,
                                float *final_state, void *out, void *workspace,
                                size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_prefill_kernel_launches -- how many kernels one kda_chunk_prefill call
+ * with these sizes and this workspace size launches (q, k, v, z and out
+ * assumed 16-byte aligned); 0 for an empty batch.  For instrumentation, e.g. a
+ * benchmark that reports its kernel launches.  Pure host computation: no
+ * device call, no error status.
+ */
+int kda_prefill_kernel_launches(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                kda_dtype_t dtype, size_t workspace_bytes);
 
 /*
  * kda_chunk_prefill_noalloc -- kda_chunk_prefill for callers that cannot
