@@ -180,49 +180,90 @@ def test_unsupported_and_invalid_arguments():
                       workspace=ws)
 
 
-def _run_both_paths(d, dev):
-    """The same call with a minimal workspace (the fused kernel) and with the
-    workspace the library asks for (the split path when the batch has few
-    chains)."""
-    from gated_delta_rule_46_gb300 import workspace_size
+def _plan_workspaces(T, N, H):
+    """Workspace sizes that select each tensor-core plan for this batch: the
+    minimum (one fused kernel), the smallest size that leaves it (the windowed
+    split plan) and the size the library asks for (the segment scan, for few
+    chains).  The plan a size selects is read from the launch count."""
+    from gated_delta_rule_46_gb300 import prefill_kernel_launches, workspace_size
+    n = lambda ws: prefill_kernel_launches(T, N, H, 128, 128, torch.bfloat16, ws)
+    small, big = 4096 + 4 * N, workspace_size(T, N, H, 128, 128)
+    assert n(small) == 2 and n(big) == 5, (n(small), n(big))
+    lo, hi = small, big
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if n(mid) == 2:
+            lo = mid
+        else:
+            hi = mid
+    hi = (hi + 255) // 256 * 256
+    assert n(hi) not in (2, 5), "the windowed plan should sit between the other two"
+    return small, hi, big
+
+
+def _run_plans(d, dev):
+    """The same call under each plan; returns {plan: (out, final)}."""
     g = to_device(d, dev)
     T, H, dk = g["q"].shape
     N = g["cu_seqlens"].shape[0] - 1
-    small = torch.zeros(4096 + 4 * N, dtype=torch.uint8, device=dev)
-    big = torch.zeros(workspace_size(T, N, H, dk, dk), dtype=torch.uint8, device=dev)
-    assert big.numel() > small.numel(), "this batch should plan the split path"
+    sizes = dict(zip(("fused", "windows", "scan"), _plan_workspaces(T, N, H)))
     args = (g["q"], g["k"], g["v"], g["z"], g["A"], g["beta"], g["cu_seqlens"], g["initial_state"])
-    of, ff = chunk_prefill(*args, workspace=small)
-    os_, fs = chunk_prefill(*args, workspace=big)
-    torch.cuda.synchronize()
-    assert check_device_status(big) == 0 and check_device_status(small) == 0
-    return (of, ff), (os_, fs)
+    res = {}
+    for plan, size in sizes.items():
+        ws = torch.zeros(size, dtype=torch.uint8, device=dev)
+        res[plan] = chunk_prefill(*args, workspace=ws)
+        torch.cuda.synchronize()
+        assert check_device_status(ws) == 0, plan
+    return res
 
 
-def test_split_path_matches_fused_and_oracle():
-    """Few chains, ragged sequences (one empty): the chunk-parallel split path
-    agrees with the oracle and with the fused kernel."""
+def test_split_plans_match_fused_and_oracle():
+    """Few chains, ragged sequences (one empty, one shorter than a segment):
+    the windowed split plan and the segment scan agree with the oracle and
+    with the fused kernel."""
     dev = need_gpu()
     w = inputs.custom([1500, 33, 900, 0, 640, 129], H=4, dk=128, dv=128, dtype=torch.bfloat16,
                       init="randn0.1", wid=21)
     d = inputs.prefill_inputs(w)
-    (of, ff), (os_, fs) = _run_both_paths(d, dev)
+    res = _run_plans(d, dev)
     ro, rf = _run_oracle(d)
-    assert_close("split out", os_, ro, torch.bfloat16)
-    assert_close("split final", fs, rf, torch.bfloat16)
-    assert_close("fused out", of, ro, torch.bfloat16)
-    assert_close("split vs fused out", os_, of.double().cpu().numpy(), torch.bfloat16)
-    assert torch.equal(fs[3], d["initial_state"][3].to(dev))   # empty sequence passes its state
+    for plan, (o, f) in res.items():
+        assert_close(f"{plan} out", o, ro, torch.bfloat16)
+        assert_close(f"{plan} final", f, rf, torch.bfloat16)
+        assert torch.equal(f[3], d["initial_state"][3].to(dev)), plan   # empty sequence passes its state
+    for plan in ("windows", "scan"):
+        assert_close(f"{plan} vs fused out", res[plan][0], res["fused"][0].double().cpu().numpy(),
+                     torch.bfloat16)
 
 
-def test_split_path_several_windows():
-    """A sequence long enough for the split path to run several windows of
-    chunks, carrying the state between them."""
+def test_split_plans_long_sequence():
+    """A sequence long enough for several windows (state carried between them)
+    and for a few dozen scan segments, next to a shorter one."""
     dev = need_gpu()
     w = inputs.custom([20000, 3000], H=2, dk=128, dv=128, dtype=torch.bfloat16, init="randn0.1", wid=22)
     d = inputs.prefill_inputs(w)
-    (of, ff), (os_, fs) = _run_both_paths(d, dev)
+    res = _run_plans(d, dev)
     ro, rf = _run_oracle(d)
-    assert_close("split out", os_, ro, torch.bfloat16)
-    assert_close("split final", fs, rf, torch.bfloat16)
-    assert_close("fused final", ff, rf, torch.bfloat16)
+    for plan, (o, f) in res.items():
+        assert_close(f"{plan} out", o, ro, torch.bfloat16)
+        assert_close(f"{plan} final", f, rf, torch.bfloat16)
+
+
+def test_slow_decay_all_plans():
+    """Gates close to 0 (z shifted down by 10, so exp(A) z is far below 0 and
+    g = -5 sigmoid(.) is small): the state keeps its memory over many chunks,
+    so the carried state, the W S correction and the segment maps of the scan
+    carry the result instead of decaying away within a chunk.  Every plan
+    against the oracle."""
+    dev = need_gpu()
+    w = inputs.custom([3000, 1100, 700], H=4, dk=128, dv=128, dtype=torch.bfloat16,
+                      init="randn0.1", wid=23)
+    d = inputs.prefill_inputs(w)
+    d["z"] = (d["z"].float() - 10.0).to(torch.bfloat16)
+    g = oracle.gate(d["z"][:256], d["A"])
+    assert (g.mean(axis=0) > -0.01).mean() > 0.3    # a third of the channels barely decay
+    res = _run_plans(d, dev)
+    ro, rf = _run_oracle(d)
+    for plan, (o, f) in res.items():
+        assert_close(f"{plan} out", o, ro, torch.bfloat16)
+        assert_close(f"{plan} final", f, rf, torch.bfloat16)
