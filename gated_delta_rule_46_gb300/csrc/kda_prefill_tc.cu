@@ -288,7 +288,7 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
         *reinterpret_cast<uint32_t *>(qk + okk) = pack_bf16(kh0, kh1);
         kt0[i] = kh0 * rho0;
         kt1[i] = kh1 * rho1;
-        *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kt0[i], kt1[i]);            // K~
+        if (!KT) *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kt0[i], kt1[i]);   // K~ (KT: as K~^T)
         *reinterpret_cast<uint32_t *>(b1 + okk) = pack_bf16(qe0 * rho0, qe1 * rho1);   // Q~
         const float fr0 = kv.x * dd0, fr1 = kv.y * dd1;                     // k 2^(R_ta - G_t)
         kr0[i] = fr0 * ke0;                                                 // k 2^(G_end - G_t)
@@ -925,8 +925,9 @@ constexpr uint32_t REC_BYTES = 74240;
 constexpr uint32_t OFF_TB_INTRA = OFF_ST;   // the intra kernel keeps T where the state tile would be
 constexpr uint32_t OFF_UT_INTRA = OFF_PB;   // U~^T staging: P (exported by then) and the unused 8 KB after it
 constexpr uint32_t OFF_NW_INTRA = OFF_VT;   // -W staging (two 64-row K-block halves), over V^T once the MMAs ran
-constexpr uint32_t TM_W = 0, TM_UT = 64;    // intra kernel: W^T and U~^T accumulators (N = 64)
+constexpr uint32_t TM_W = 0, TM_UT = 128;   // intra kernel: W [t][c] (N = 128) and U~^T (N = 64)
 static_assert(OFF_KT + 16384 <= OFF_MISC, "K~^T tile overlaps");
+static_assert(OFF_TB_INTRA + 8192 == OFF_KT, "the W MMA reads 128 rows from the T tile on");
 static_assert(OFF_UT_INTRA + 16384 <= OFF_GB && OFF_NW_INTRA + 16384 <= OFF_PB, "staging overlaps");
 
 struct SplitParams {
@@ -1002,21 +1003,25 @@ __device__ __forceinline__ bool item_info(const SplitParams &p, int it, ItemInfo
     return true;
 }
 
-// W^T and U~^T out of TMEM into their staging tiles: -W as the two 64-row
-// K-block halves of the [-W; Q~] operand, U~^T [j][t].
+// W and U~^T out of TMEM into their staging tiles: -W [t][c] as the two 64-row
+// K-block halves of the [-W; Q~] operand (lanes t < 64, 32 columns per
+// thread), U~^T [j][t] (all lanes, 16 columns per thread).
 __device__ __forceinline__ void phase_wu_out(const Ctx &x) {
-    float Wt[16], Ut[16];
-    ptx::tmem_ld16(x.lane_base + TM_W + 16 * x.cg, Wt);    // W^T[c][16 cg + i], c = ch
+    if (x.qw < 2) {
+        float Wr[32];
+        ptx::tmem_ld32(x.lane_base + TM_W + 32 * x.cg, Wr);   // W[t][32 cg + i], t = ch
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) Wr[i] = -Wr[i];
+        uint8_t *nw = x.sm + OFF_NW_INTRA + (x.cg >> 1) * 8192;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) st_chunk(nw, swz(x.ch, 4 * (x.cg & 1) + q4), Wr + 8 * q4);
+    }
+    float Ut[16];
     ptx::tmem_ld16(x.lane_base + TM_UT + 16 * x.cg, Ut);   // U~^T[j][16 cg + i], j = ch
     ptx::tmem_ld_wait();
-    const int c = x.ch;
-    uint8_t *b1 = x.sm + OFF_NW_INTRA + (c >> 6) * 8192;
-    const uint32_t cc = (uint32_t)((c & 63) >> 3), ci = (uint32_t)(c & 7) * 2u;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<__nv_bfloat16 *>(b1 + swz(16 * x.cg + i, cc) + ci) = __float2bfloat16_rn(-Wt[i]);
-    st_chunk(x.sm + OFF_UT_INTRA, swz(c, 2 * x.cg), Ut);
-    st_chunk(x.sm + OFF_UT_INTRA, swz(c, 2 * x.cg + 1), Ut + 8);
+    st_chunk(x.sm + OFF_UT_INTRA, swz(x.ch, 2 * x.cg), Ut);
+    st_chunk(x.sm + OFF_UT_INTRA, swz(x.ch, 2 * x.cg + 1), Ut + 8);
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -1139,9 +1144,10 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (tid == 0) {
             ptx::tc_fence_after_sync();
             ptx::bulk_wait_read();   // P has left its tile (U~^T staging goes there)
-            // W^T[c][t] = K~^T[c] . T[t] and U~^T[j][t] = V^T[j] . T[t]
-            mma_k<4>(tmem + TM_W, sbase + OFF_KT, 0u, sbase + OFF_TB_INTRA, 0u,
-                     ptx::idesc_bf16_f32(128, 64), false);
+            // W[t][c] = T[t] . K~^T[c] (rows t >= 64 of the left operand run over
+            // the next tile and are discarded) and U~^T[j][t] = V^T[j] . T[t]
+            mma_k<4>(tmem + TM_W, sbase + OFF_TB_INTRA, 0u, sbase + OFF_KT, 0u,
+                     ptx::idesc_bf16_f32(128, 128), false);
             mma_k<4>(tmem + TM_UT, sbase + OFF_VT, 0u, sbase + OFF_TB_INTRA, 0u,
                      ptx::idesc_bf16_f32(128, 64), false);
             ptx::mma_commit(bar_g);
