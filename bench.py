@@ -339,7 +339,10 @@ def run_gpu(args):
                 "traffic": _ncu_traffic("decode_kernel", "kda_simt.cu"),
                 "algorithmic_bytes_per_launch": alg_dec, "peak_source": peak_kind,
                 "us_per_launch": per_launch_dec * 1e6}
-    roof_pref = {"kernel": f"kda_chunk_prefill ({L_pref} launches: schedule, then intra-chunk and state-pass kernel per window)", "bound": "hbm",
+    plan = {2: "schedule + fused prefill_tc_kernel",
+            5: "schedule, intra-chunk, segment maps, scan, segment state pass"}.get(
+                L_pref, "schedule, then an intra-chunk and a state-pass kernel per window")
+    roof_pref = {"kernel": f"kda_chunk_prefill ({L_pref} launches: {plan})", "bound": "hbm",
                  "achieved": ach_pref, "peak": peak, "unit": "GB/s", "frac": ach_pref / peak,
                  "traffic": _ncu_traffic("kda_chunk_prefill_T4096_H16", "kda_prefill_tc.cu"),
                  "algorithmic_bytes_per_launch": alg_pref, "peak_source": peak_kind,

@@ -27,19 +27,20 @@
 // earlier tiles.  Both factors are finite in float32 and bf16, so one dense
 // MMA per row tile covers its diagonal and off-diagonal blocks.
 //
-// One CTA (256 threads, 8 warps) per SM, persistent over (sequence, head)
-// chains taken longest-first from a device work counter.  Per chunk:
-//   A  SIMT: gate, cumulative decay, operand tiles (bf16, 128B-swizzled)
-//      MMA: Gram/P tiles [Q^;K^] x B_a^T (4 tiles) and S^T x [K~;Q~]^T
-//   B  SIMT: mask P and L from TMEM, RHS^T = V^T - (K~S0)^T, blocked
-//      forward substitution for T
-//      MMA: U^T = RHS^T T^T
-//   C  SIMT: U^T -> bf16 operand
-//      MMA: O^T += U^T P^T ; dS^T = U^T Kend^T
-//   D  SIMT: S^T = S^T Diag(e^{G_end}) + dS^T (float32 master in registers),
-//      bf16 copy of S^T for the next chunk, O stored to global memory
-// The state is kept transposed (rows = value channels) so every accumulator
-// has M = 128 rows, one per TMEM lane.
+// Every kernel here runs 512 threads (16 warps) per CTA, one CTA per SM, with
+// bf16 operands in 128-byte-swizzled K-major shared-memory tiles and float32
+// accumulators in TMEM.  Per 64-token chunk:
+//   A    SIMT: gate, cumulative decay, operand tiles (phase_gate_operands)
+//   MMA  Gram/P tiles [Q^;K^] x B_a^T (one N = 160 chain)
+//   B    P and L out of TMEM, the inverse T = (I + L)^{-1} Diag(beta): diagonal
+//        blocks in float32 SIMT, the rest on warp-level tf32 MMAs
+//   then the state pass: U, O = Q~S0 + PU and the new state on tcgen05.
+// The state is kept transposed (rows = value channels) so every state
+// accumulator has M = 128 rows, one per TMEM lane.  Plans (host code at the
+// end): the fused persistent kernel for batches whose chains fill the GPU; for
+// few chains the state-independent work runs chunk-parallel in
+// prefill_intra_kernel and the state pass either window by window or as a
+// segment scan (pass 1, scan, pass 2).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

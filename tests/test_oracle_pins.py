@@ -16,6 +16,9 @@ against things other than itself:
 * two independently derived formulations: the generalised-Householder product
   form with explicit dense matrices, and the chunkwise WY/UT form (the algebra
   the GPU kernels implement) for chunk sizes 1, 4, 16 and 64 with ragged tails;
+* the affine segment maps behind the GPU's segment scan: the chunk-formula
+  transition M equals the map the oracle realises, and composing segments
+  with S_in(g+1) = M_g S_in(g) + S0_g reproduces a single call;
 * structural properties: packed sequences are independent, a split resumed
   from the carried state equals one call, T decode steps equal a T-token
   prefill, and the norm bound ||S_t|| <= ||S_{t-1}|| + beta ||v_t||;
@@ -266,6 +269,61 @@ def test_chunked_wy_form_unit_decay_and_zero_state():
     co, cf = _chunked_form(p, g, 16)
     np.testing.assert_allclose(out, co, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(fin, cf, rtol=1e-10, atol=1e-12)
+
+
+def _segment_map(p, g, h, t0, t1, C):
+    """Transition of the state over tokens [t0, t1) (whole chunks of C from t0),
+    by the chunk formula the GPU's segment pass propagates:
+    M = prod_chunks (Diag(e^{G_end}) - Kend^T T K~), later chunks on the left."""
+    k, beta = p["k"].astype(np.float64), p["beta"].astype(np.float64)
+    dk = k.shape[2]
+    M = np.eye(dk)
+    for c0 in range(t0, t1, C):
+        c1 = min(c0 + C, t1)
+        n = c1 - c0
+        K, b = k[c0:c1, h], beta[c0:c1, h]
+        G = np.cumsum(g[c0:c1, h], axis=0)
+        diff = G[:, None, :] - G[None, :, :]
+        D = np.exp(np.where(np.tril(np.ones((n, n), bool))[:, :, None], diff, -np.inf))
+        L = np.tril(np.einsum("tc,sc,tsc->ts", K, K, D), -1) * b[:, None]
+        Tm = np.linalg.solve(np.eye(n) + L, np.diag(b))
+        W = Tm @ (K * np.exp(G))
+        Kend = K * np.exp(G[-1][None, :] - G)
+        M = (np.diag(np.exp(G[-1])) - Kend.T @ W) @ M
+    return M
+
+
+def test_segment_maps_compose_affinely():
+    """The state map over a segment is affine, S_out = M S_in + S0, with M the
+    chunk-formula product above and S0 the segment run from a zero state; the
+    scan S_in(g+1) = M_g S_in(g) + S0_g over three segments reproduces the
+    whole sequence's final state and, resumed from S_in(g), its outputs.  Slow
+    decay (g near 0) and small beta keep M far from 0 so every term matters."""
+    rng = np.random.default_rng(11)
+    dk = dv = 6
+    lens, H, C = [96], 1, 16
+    p = _rand_problem(rng, lens, H, dk, dv)
+    p["beta"] = (0.05 * p["beta"]).astype(np.float32)   # gentle writes: the delta rule forgets slowly too
+    g = -0.02 * np.abs(rng.standard_normal((96, H, dk)))
+    out, fin = _run(p, g=g)
+    S = p["s0"][0, 0].copy()
+    for t0, t1 in [(0, 32), (32, 80), (80, 96)]:
+        sub = {n: (p[n][t0:t1] if n in ("q", "k", "v", "z", "beta") else p[n]) for n in p}
+        sub["cu"] = np.array([0, t1 - t0], dtype=np.int64)
+        gs = g[t0:t1]
+        M = _segment_map(p, g, 0, t0, t1, C)
+        assert np.abs(M).max() > 0.2                                  # far from decayed away
+        sub["s0"] = np.zeros((1, H, dk, dv))
+        _, S0 = _run(sub, g=gs)
+        sub["s0"] = np.eye(dk)[None, None]                            # dv = dk: S_in = I gives M + S0
+        _, SI = _run(sub, g=gs)
+        np.testing.assert_allclose(SI[0, 0] - S0[0, 0], M, rtol=1e-9, atol=1e-11)
+        sub["s0"] = S[None, None]
+        seg_out, seg_fin = _run(sub, g=gs)
+        np.testing.assert_allclose(seg_out, out[t0:t1], rtol=1e-9, atol=1e-11)
+        S = M @ S + S0[0, 0]                                          # the scan step
+        np.testing.assert_allclose(seg_fin[0, 0], S, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(S, fin[0, 0], rtol=1e-9, atol=1e-11)
 
 
 # --------------------------------------------------------------------------- structure
