@@ -348,6 +348,10 @@ def run_gpu(args):
                  "algorithmic_bytes_per_launch": alg_pref, "peak_source": peak_kind,
                  "us_per_launch": per_launch_pref * 1e6}
 
+    # ---- the decode workload through kda_decode_tokens: 8 tokens per call from a
+    # slot pool (the 256 states scattered over 512 slots), 16 calls = 128 tokens
+    multi = _time_decode_tokens(kda, inputs, w4, dev, seed, barrier, agg_max, peak, peak_kind)
+
     # ---- the two large prefill workloads, inputs generated on the device
     extra = {}
     if not args.no_extra_workloads:
@@ -383,8 +387,9 @@ def run_gpu(args):
             "e2e": {"value": pref_tokens / e2p, "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d_pref + h2d_dec, "d2h_bytes_per_step": d2h_pref + d2h_dec,
                     "decode_value": dec_tokens / e2d},
+            "decode_tokens": multi,
             "prefill_large": extra,
-            "gpu_launches": K * (L_pref + NS),
+            "gpu_launches": K * (L_pref + NS),   # the timed step; decode_tokens and prefill_large are timed apart
             "clocks": clk.result,
             "device_status": ok_status,
             "cpu_baseline": cpu,
@@ -394,6 +399,60 @@ def run_gpu(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def _time_decode_tokens(kda, inputs, w4, dev, seed, barrier, agg_max, peak, peak_kind,
+                        n_tok=8, reps=3):
+    """The decode workload's 256 sequences x 32 heads stepped n_tok tokens per
+    kda_decode_tokens call through a pool of 512 slots (a seeded permutation
+    names each sequence's slot), 128 / n_tok calls per pass: the state is read
+    and written once per call instead of once per token."""
+    import torch
+    N, H, d = w4.decode_N, w4.H, 128
+    calls = w4.decode_steps // n_tok
+    g = torch.Generator(device=dev)
+    g.manual_seed(2000 + seed)
+
+    def normal(shape):
+        return torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+
+    q = torch.nn.functional.normalize(normal((calls, N, n_tok, H, d)), dim=-1).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(normal((calls, N, n_tok, H, d)), dim=-1).to(torch.bfloat16)
+    v = normal((calls, N, n_tok, H, d)).to(torch.bfloat16)
+    z = normal((calls, N, n_tok, H, d)).to(torch.bfloat16)
+    beta = torch.sigmoid(normal((calls, N, n_tok, H)))
+    A = torch.rand((H, d), generator=g, device=dev) * 2 - 1
+    pool = 0.1 * normal((2 * N, H, d, d))
+    slots = torch.randperm(2 * N, generator=g, device=dev)[:N].to(torch.int32)
+    out = torch.empty((N, n_tok, H, d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run_pass():
+        for c in range(calls):
+            kda.decode_tokens(q[c], k[c], v[c], z[c], A, beta[c], pool, slot_ids=slots, out=out)
+
+    run_pass()
+    barrier()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run_pass()
+        e1.record(stream)
+        barrier()
+        times.append(e0.elapsed_time(e1) / 1000.0)
+    t = agg_max(min(times))
+    per_call = t / calls
+    alg = N * H * (2 * d * d * 4 + n_tok * inputs.bytes_per_token_head(d, d, 2)) + H * d * 4 + 4 * N
+    ach = alg / per_call / 1e9
+    del q, k, v, z, beta, pool
+    torch.cuda.empty_cache()
+    return {"workload": f"decode {N} seqs x {w4.decode_steps} tokens, H={H}, d={d}, bf16, {n_tok} tokens "
+                        f"per kda_decode_tokens call, states in a {2 * N}-slot pool",
+            "value": N * w4.decode_steps / t, "unit": "tokens/s", "us_per_call": per_call * 1e6,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                         "frac": ach / peak, "algorithmic_bytes_per_launch": alg,
+                         "peak_source": peak_kind}}
 
 
 # Prefill cases timed on their own (`--case`), e.g. as the command an ncu

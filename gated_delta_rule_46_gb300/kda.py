@@ -54,6 +54,8 @@ def lib():
             L.kda_chunk_prefill.restype = I
             L.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P]
             L.kda_decode_step.restype = I
+            L.kda_decode_tokens.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, P, P]
+            L.kda_decode_tokens.restype = I
             L.kda_prefill_kernel_launches.argtypes = [I64, I, I, I, I, I, SZ]
             L.kda_prefill_kernel_launches.restype = I
             L.kda_check_device_status.argtypes = [P, P]
@@ -156,6 +158,39 @@ def chunk_prefill(q, k, v, z, A, beta, cu_seqlens, initial_state=None, final_sta
                                  _ptr(workspace), workspace.numel(), _stream(stream))
     _raise(st, "kda_chunk_prefill")
     return out, final_state
+
+
+def decode_tokens(q, k, v, z, A, beta, state_pool, slot_ids=None, out=None, status=None,
+                  stream=None):
+    """n new tokens for each of N sequences, states in a pool (updated in place).
+
+    q, k, z [N, n, H, dk]; v [N, n, H, dv]; beta [N, n, H] f32; state_pool
+    [P, H, dk, dv] f32; slot_ids [N] int32 (device) or None for slot i = i;
+    a negative slot is a padding row.  status: optional device uint32 tensor
+    (e.g. a prefill workspace) that records ids >= P.  Returns out [N, n, H, dv].
+    """
+    _check(q, "q")
+    N, n, H, dk = q.shape
+    dv = v.shape[3] if v.dim() == 4 else -1
+    dev = q.device
+    for name, t in (("k", k), ("z", z)):
+        _check(t, name, (N, n, H, dk), q.dtype, dev)
+    _check(v, "v", (N, n, H, dv), q.dtype, dev)
+    _check(A, "A", (H, dk), torch.float32, dev)
+    _check(beta, "beta", (N, n, H), torch.float32, dev)
+    _check(state_pool, "state_pool", None, torch.float32, dev)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"state_pool must be [P, {H}, {dk}, {dv}], got {tuple(state_pool.shape)}")
+    if slot_ids is not None:
+        _check(slot_ids, "slot_ids", (N,), torch.int32, dev)
+    if out is None:
+        out = torch.empty((N, n, H, dv), dtype=q.dtype, device=dev)
+    _check(out, "out", (N, n, H, dv), q.dtype, dev)
+    st = lib().kda_decode_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                 _ptr(state_pool), state_pool.shape[0], _ptr(slot_ids), _ptr(out),
+                                 N, n, H, dk, dv, _dtype_code(q), _ptr(status), _stream(stream))
+    _raise(st, "kda_decode_tokens")
+    return out
 
 
 def prefill_kernel_launches(total_tokens, num_seqs, H, dk, dv, dtype, workspace_bytes) -> int:

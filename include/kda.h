@@ -187,6 +187,37 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
                              kda_stream_t stream);
 
 /*
+ * kda_decode_tokens -- n_tokens new tokens for each of N sequences whose
+ * recurrent states live in a pool, as a serving engine keeps them (the
+ * fixed-size state that replaces the KV cache, "Sequence mixing": one state
+ * per live sequence, stepped in batches).  Sequence i applies its tokens in
+ * order to state_pool[slot_ids[i]], updated in place; every token gets its
+ * output.  With n_tokens > 1 the state is read and written once per call, not
+ * once per token.  kda_decode_step is the case n_tokens = 1, slot i = i.
+ *   q, k, z     [N, n_tokens, H, dk], element type dtype
+ *   v           [N, n_tokens, H, dv], element type dtype
+ *   A           [H, dk] float32
+ *   beta        [N, n_tokens, H] float32
+ *   state_pool  [pool_size, H, dk, dv] float32, 16-byte aligned, read and
+ *               overwritten at the slots named
+ *   slot_ids    [N] int32, device, or NULL for slot i = sequence i (then
+ *               pool_size >= N).  A negative id marks a padding row: its
+ *               outputs are written as zeros and no state is touched.  An id
+ *               >= pool_size is recorded in *status (KDA_ERR_INVALID_ARG) and
+ *               its row is treated as padding.  Two rows of one call naming
+ *               the same slot race; give each live sequence its own slot.
+ *   out         [N, n_tokens, H, dv], element type dtype (written)
+ *   status      device uint32, or NULL; e.g. the first word of a prefill
+ *               workspace, then read with kda_check_device_status()
+ * Supported: dk, dv in {32, 64, 128}, any n_tokens >= 0.
+ */
+kda_status_t kda_decode_tokens(const void *q, const void *k, const void *v, const void *z,
+                               const float *A, const float *beta, float *state_pool,
+                               int pool_size, const int32_t *slot_ids, void *out, int N,
+                               int n_tokens, int H, int dk, int dv, kda_dtype_t dtype,
+                               uint32_t *status, kda_stream_t stream);
+
+/*
  * kda_check_device_status -- synchronises `stream`, reads the status word that
  * kda_chunk_prefill keeps in `workspace`, and returns KDA_OK or the recorded
  * device-side error (KDA_ERR_DEVICE_TIMEOUT).  Returns KDA_ERR_CUDA if the

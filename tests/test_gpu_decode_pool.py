@@ -1,0 +1,90 @@
+"""kda_decode_tokens (several tokens per sequence, states in a slot-indexed
+pool) against the oracle, against repeated kda_decode_step calls, and its
+handling of padding rows and bad slot ids."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_46_gb300 import KDAError, decode_step, decode_tokens, inputs, kda
+from gpu_util import assert_close, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _batch(N, n, H, dk, dv, dtype, wid):
+    """N sequences of n new tokens each, as [N, n, H, d] tensors (seeded)."""
+    w = inputs.custom([n] * N, H=H, dk=dk, dv=dv, dtype=dtype, wid=wid)
+    d = inputs.prefill_inputs(w)
+    shp = lambda t, last: t.reshape(N, n, H, last)
+    return {"q": shp(d["q"], dk), "k": shp(d["k"], dk), "v": shp(d["v"], dv), "z": shp(d["z"], dk),
+            "beta": d["beta"].reshape(N, n, H), "A": d["A"], "flat": d, "cu": d["cu_seqlens"]}
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.float32, 64, 32)])
+def test_pool_slots_multi_token_against_oracle(dtype, dk, dv):
+    dev = need_gpu()
+    N, n, H, P = 6, 5, 3, 9
+    slots = [3, 7, -1, 0, 8, 5]                   # one padding row; slots 1, 2, 4, 6 untouched
+    b = _batch(N, n, H, dk, dv, dtype, wid=41)
+    rng = np.random.default_rng(41)
+    pool = torch.from_numpy((0.1 * rng.standard_normal((P, H, dk, dv))).astype(np.float32))
+    pool_dev = pool.to(dev)
+    out = decode_tokens(*(b[x].to(dev) for x in ("q", "k", "v", "z", "A", "beta")), pool_dev,
+                        slot_ids=torch.tensor(slots, dtype=torch.int32, device=dev))
+    torch.cuda.synchronize()
+    # the oracle: each row's n tokens as one sequence, starting from its slot's state
+    init = np.stack([pool[max(s, 0)].double().numpy() for s in slots])
+    f = b["flat"]
+    ro, rf = oracle.prefill(f["q"], f["k"], f["v"], f["z"], f["A"], f["beta"], f["cu_seqlens"], init)
+    ro = ro.reshape(N, n, H, dv)
+    live = [i for i, s in enumerate(slots) if s >= 0]
+    assert_close("outputs", out[live], ro[live], dtype)
+    assert torch.count_nonzero(out[2]) == 0                      # padding row
+    got = pool_dev.cpu()
+    assert_close("states", got[[slots[i] for i in live]], rf[live], dtype)
+    for s in (1, 2, 4, 6):
+        assert torch.equal(got[s], pool[s]), s                   # untouched slots
+
+
+def test_tokens_equal_repeated_decode_steps():
+    """One call over 12 tokens equals 12 kda_decode_step calls (float32)."""
+    dev = need_gpu()
+    N, n, H, d = 8, 12, 2, 64
+    b = _batch(N, n, H, d, d, torch.float32, wid=42)
+    rng = np.random.default_rng(42)
+    s0 = torch.from_numpy((0.1 * rng.standard_normal((N, H, d, d))).astype(np.float32)).to(dev)
+    g = {x: b[x].to(dev) for x in ("q", "k", "v", "z", "A", "beta")}
+    pool = s0.clone()
+    out = decode_tokens(g["q"], g["k"], g["v"], g["z"], g["A"], g["beta"], pool)
+    state = s0.clone()
+    steps = [decode_step(g["q"][:, t].contiguous(), g["k"][:, t].contiguous(), g["v"][:, t].contiguous(),
+                         g["z"][:, t].contiguous(), g["A"], g["beta"][:, t].contiguous(), state)
+             for t in range(n)]
+    torch.cuda.synchronize()
+    ref = torch.stack(steps, dim=1)
+    assert torch.allclose(out, ref, rtol=1e-5, atol=1e-6)
+    assert torch.allclose(pool, state, rtol=1e-5, atol=1e-6)
+
+
+def test_bad_slot_is_recorded_and_skipped():
+    dev = need_gpu()
+    N, n, H, d, P = 3, 2, 2, 32, 4
+    b = _batch(N, n, H, d, d, torch.float32, wid=43)
+    pool = torch.ones((P, H, d, d), dtype=torch.float32, device=dev)
+    status = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = decode_tokens(*(b[x].to(dev) for x in ("q", "k", "v", "z", "A", "beta")), pool,
+                        slot_ids=torch.tensor([0, 9, 2], dtype=torch.int32, device=dev), status=status)
+    assert kda.check_device_status(status) == kda.KDA_ERR_INVALID_ARG
+    assert torch.count_nonzero(out[1]) == 0
+    assert torch.equal(pool[1], torch.ones_like(pool[1])) and torch.equal(pool[3], torch.ones_like(pool[3]))
+    assert not torch.equal(pool[0], torch.ones_like(pool[0]))
+
+
+def test_invalid_arguments():
+    dev = need_gpu()
+    b = _batch(2, 1, 1, 32, 32, torch.float32, wid=44)
+    g = [b[x].to(dev) for x in ("q", "k", "v", "z", "A", "beta")]
+    small = torch.zeros((1, 1, 32, 32), dtype=torch.float32, device=dev)
+    with pytest.raises(KDAError):          # no slot ids and a pool smaller than N
+        decode_tokens(*g, small)
