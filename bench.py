@@ -120,6 +120,18 @@ class ClockSampler:
         return False
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (the slowest rank's time): one all-reduce
+    on `device` (the GPU under NCCL, the CPU under gloo); x itself when alone."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -307,11 +319,7 @@ def run_gpu(args):
     e2e_dec = [ee[i][2].elapsed_time(ee[i][3]) for i in range(K)]
 
     def agg_max(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, world, dev)
 
     tp = agg_max(sum(t_pref) / 1000.0)
     td = agg_max(sum(t_dec) / 1000.0)
