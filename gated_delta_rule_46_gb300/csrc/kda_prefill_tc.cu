@@ -750,6 +750,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     const Ctx x = make_ctx(sm, tmem);
+    ptx::pdl_wait();                 // the schedule kernel's order, counter and status
+    ptx::pdl_launch_dependents();
 
     // issue / completion counters of the barriers (uniform across threads);
     // a barrier's next expected phase parity is (done & 1)
@@ -1042,11 +1044,6 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5;
     const int H = p.H;
 
-    // bad sequence offsets are reported once, by the first CTA
-    if (blockIdx.x == 0 && tid < p.num_seqs) {
-        const int64_t b = p.cu_seqlens[tid], e = p.cu_seqlens[tid + 1];
-        if (b < 0 || e < b || e > p.total_tokens) report_status(p.status, kDevBadSeqlens);
-    }
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) ptx::mbar_init(bar_qk + i, 1);
         ptx::fence_mbar_init();
@@ -1061,6 +1058,13 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     const Ctx x = make_ctx(sm, tmem);
+    ptx::pdl_wait();                 // the previous kernel's status word (and, windowed, nothing else)
+    ptx::pdl_launch_dependents();
+    // bad sequence offsets are reported once, by the first CTA
+    if (blockIdx.x == 0 && tid < p.num_seqs) {
+        const int64_t b = p.cu_seqlens[tid], e = p.cu_seqlens[tid + 1];
+        if (b < 0 || e < b || e > p.total_tokens) report_status(p.status, kDevBadSeqlens);
+    }
 
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
     uint32_t g_issued = 0, g_done = 0;
@@ -1280,6 +1284,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     Ctx x = make_ctx(sm, tmem);
+    ptx::pdl_wait();                 // records, incoming states of the previous kernels
+    ptx::pdl_launch_dependents();
     const uint8_t *recs = p.records + (size_t)chain * p.W * REC_BYTES;
 
     uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
@@ -1498,6 +1504,8 @@ prefill_seg_kernel(const SplitParams p) {
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     const Ctx x = make_ctx(sm, tmem);
+    ptx::pdl_wait();                 // the intra kernel's records
+    ptx::pdl_launch_dependents();
     const uint8_t *recs = p.records + (size_t)chain * p.W * REC_BYTES;
 
     uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
@@ -1625,6 +1633,8 @@ prefill_scan_kernel(const SplitParams p) {
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     const Ctx x = make_ctx(sm, tmem);
+    ptx::pdl_wait();                 // the segment maps
+    ptx::pdl_launch_dependents();
     const int64_t sidx = (int64_t)chain * D * D;
     const uint8_t *cells = p.seg_out + (size_t)chain * p.segs * SEG_CELL;
     uint32_t issued = 0, done = 0, mb_issued[2] = {0, 0}, mb_done[2] = {0, 0};
@@ -1851,6 +1861,25 @@ static cudaError_t side_stream(SideStream **out) {
 cudaError_t launch_schedule(const int32_t *cu, int num_seqs, int32_t *order, uint32_t *counter,
                             uint32_t *status, cudaStream_t st);
 
+// Launches a kernel with programmatic stream serialization: it may start
+// while the previous kernel of the stream finishes and waits for that
+// kernel's results in ptx::pdl_wait().
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned smem,
+                              cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(tc::NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
@@ -1892,13 +1921,15 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.seg_out = ws + scan.seg_out_off;
         sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
         const int64_t items = chains * scan.max_chunks;
-        tc::prefill_intra_kernel<<<(int)(items < sms ? items : sms), tc::NT, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mz, sp);
+        if ((e = launch_pdl(tc::prefill_intra_kernel, (unsigned)(items < sms ? items : sms),
+                            tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
+            return e;
         sp.segs = scan.segs;
         const unsigned cells = (unsigned)(chains * scan.segs);
-        tc::prefill_seg_kernel<<<cells, tc::NT, tc::SMEM_SEG, st>>>(sp);
-        tc::prefill_scan_kernel<<<(unsigned)chains, tc::NT, tc::SMEM_SCAN, st>>>(sp);
-        tc::prefill_state_kernel<<<cells, tc::NT, tc::SMEM_STATE, st>>>(mo, sp);
-        return cudaGetLastError();
+        if ((e = launch_pdl(tc::prefill_seg_kernel, cells, tc::SMEM_SEG, st, sp)) != cudaSuccess) return e;
+        if ((e = launch_pdl(tc::prefill_scan_kernel, (unsigned)chains, tc::SMEM_SCAN, st, sp)) != cudaSuccess)
+            return e;
+        return launch_pdl(tc::prefill_state_kernel, cells, tc::SMEM_STATE, st, mo, sp);
     }
 
     const SplitPlan plan = plan_split(total, num_seqs, H);
@@ -1954,8 +1985,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
     prm.counter = counter; prm.status = status; prm.total_tokens = total;
     prm.num_seqs = num_seqs; prm.H = H;
-    tc::prefill_tc_kernel<<<grid, tc::NT, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mz, mo, prm);
-    return cudaGetLastError();
+    return launch_pdl(tc::prefill_tc_kernel, (unsigned)grid, tc::SMEM_ALLOC, st, mq, mk, mv, mz, mo, prm);
 }
 
 }  // namespace kda

@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
                                                         uint32_t *counter, uint32_t *status) {
     __shared__ int64_t s_key[kSortMax];
     const int tid = threadIdx.x;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the prefill kernel may start its setup
     if (tid == 0) { *counter = 0u; *status = kDevOk; }
     if (num_seqs > kSortMax) {
         for (int i = tid; i < num_seqs; i += blockDim.x) order[i] = i;

@@ -52,6 +52,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
     return true;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// Waits until the grids this one depends on (the previous kernel of the stream,
+// when launched with programmatic stream serialization) have completed and
+// their memory is visible; returns at once otherwise.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel of the stream start its blocks before this grid ends
+// (it still waits in pdl_wait for this grid's completion before using its data).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
