@@ -360,6 +360,11 @@ def run_gpu(args):
     # slot pool (the 256 states scattered over 512 slots), 16 calls = 128 tokens
     multi = _time_decode_tokens(kda, inputs, w4, dev, seed, barrier, agg_max, peak, peak_kind)
 
+    # ---- ablation: the same prefill through the unbounded log-decay entry point
+    # (token-serial kernel), g taken from the bounded gate so both compute one layer
+    ablation = _time_unbounded_gate(kda, g1, fin1, out1, ws1, flush, barrier, agg_max, stream,
+                                    T1, tp / K)
+
     # ---- the two large prefill workloads, inputs generated on the device
     extra = {}
     if not args.no_extra_workloads:
@@ -397,6 +402,7 @@ def run_gpu(args):
                     "decode_value": dec_tokens / e2d},
             "decode_tokens": multi,
             "prefill_large": extra,
+            "prefill_unbounded_gate": ablation,
             "gpu_launches": K * (L_pref + NS),   # the timed step; decode_tokens and prefill_large are timed apart
             "clocks": clk.result,
             "device_status": ok_status,
@@ -461,6 +467,36 @@ def _time_decode_tokens(kda, inputs, w4, dev, seed, barrier, agg_max, peak, peak
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                          "frac": ach / peak, "algorithmic_bytes_per_launch": alg,
                          "peak_source": peak_kind}}
+
+
+def _time_unbounded_gate(kda, g1, fin1, out1, ws1, flush, barrier, agg_max, stream, T1,
+                        t_bounded, reps=5):
+    """The 4096-token prefill through kda_chunk_prefill_logdecay on g = the
+    bounded gate's output: the token-serial kernel that an unbounded log-decay
+    needs, against the chunked tensor-core path that the bound allows."""
+    import torch
+    g = kda.gate(g1["z"], g1["A"])
+
+    def call():
+        kda.chunk_prefill_logdecay(g1["q"], g1["k"], g1["v"], g, g1["beta"], g1["cu_seqlens"],
+                                   g1["initial_state"], final_state=fin1, out=out1, workspace=ws1)
+
+    call()
+    barrier()
+    times = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        barrier()
+        times.append(e0.elapsed_time(e1) / 1000.0)
+    t = agg_max(min(times))
+    return {"workload": f"the same prefill (T={T1}) with the log-decay passed in (g from the bounded "
+                        "gate), token-serial kernel; the L2 flushed before each call",
+            "us_per_call": t * 1e6, "value": T1 / t, "unit": "tokens/s",
+            "bounded_chunked_us_per_call": t_bounded * 1e6}
 
 
 # Prefill cases timed on their own (`--case`), e.g. as the command an ncu

@@ -17,7 +17,7 @@ cudaError_t launch_prefill_serial(const void *q, const void *k, const void *v, c
                                   const float *A, const float *beta, const int32_t *cu,
                                   int num_seqs, int64_t total, int H, int dk, int dv, bool bf16,
                                   const float *s0, float *s1, void *out, uint32_t *status,
-                                  cudaStream_t st);
+                                  cudaStream_t st, const float *g = nullptr);
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
@@ -128,6 +128,31 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
     return from_cuda(kda::launch_prefill_serial(q, k, v, z, A, beta, cu_seqlens, num_seqs,
                                                 total_tokens, H, dk, dv, dtype == KDA_BF16,
                                                 initial_state, final_state, out, status, st));
+}
+
+kda_status_t kda_chunk_prefill_logdecay(const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta,
+                                        const int32_t *cu_seqlens, int num_seqs,
+                                        int64_t total_tokens, int H, int dk, int dv,
+                                        kda_dtype_t dtype, const float *initial_state,
+                                        float *final_state, void *out, void *workspace,
+                                        size_t workspace_bytes, kda_stream_t stream) {
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || dk <= 0 || dv <= 0)
+        return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens >= (int64_t(1) << 31) || (int64_t)num_seqs * H >= (int64_t(1) << 31))
+        return KDA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 16) || workspace_bytes < 4) return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t *status = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + kda::kWsStatus);
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return KDA_ERR_CUDA;
+    return from_cuda(kda::launch_prefill_serial(q, k, v, nullptr, nullptr, beta, cu_seqlens,
+                                                num_seqs, total_tokens, H, dk, dv,
+                                                dtype == KDA_BF16, initial_state, final_state, out,
+                                                status, st, g));
 }
 
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const void *z,

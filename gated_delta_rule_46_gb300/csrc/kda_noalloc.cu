@@ -22,7 +22,7 @@ cudaError_t launch_prefill_serial(const void *q, const void *k, const void *v, c
                                   const float *A, const float *beta, const int32_t *cu,
                                   int num_seqs, int64_t total, int H, int dk, int dv, bool bf16,
                                   const float *s0, float *s1, void *out, uint32_t *status,
-                                  cudaStream_t st);
+                                  cudaStream_t st, const float *g = nullptr);
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,

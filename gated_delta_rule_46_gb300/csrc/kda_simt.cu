@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(128) prefill_serial_kernel(
     const T *__restrict__ z, const float *__restrict__ A, const float *__restrict__ beta,
     const int32_t *__restrict__ cu_seqlens, int64_t total_tokens, int H, int dv,
     const float *__restrict__ initial_state, float *__restrict__ final_state,
-    T *__restrict__ out, uint32_t *status) {
+    T *__restrict__ out, uint32_t *status, const float *__restrict__ g_direct) {
     constexpr int TB = 16;                 // tokens staged per round
     constexpr int RPT = DK / 4;            // state rows per thread
     constexpr int PAD = DK + DK / 32;      // padded row so the 4 row groups hit distinct banks
@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(128) prefill_serial_kernel(
 #pragma unroll
     for (int i = 0; i < RPT; ++i)
         S[i] = initial_state ? initial_state[sbase + (int64_t)(cbase + i) * dv + j] : 0.f;
-    for (int c = tid; c < DK; c += 128) s_eA[c] = expf(A[h * DK + c]);
+    if (!g_direct)
+        for (int c = tid; c < DK; c += 128) s_eA[c] = expf(A[h * DK + c]);
 
     for (int64_t t0 = bos; t0 < eos; t0 += TB) {
         const int nt = (int)((eos - t0) < TB ? (eos - t0) : TB);
@@ -196,7 +197,8 @@ __global__ void __launch_bounds__(128) prefill_serial_kernel(
             const int tt = e / DK, c = e % DK;
             const int64_t idx = ((t0 + tt) * H + h) * DK + c;
             const int pc = c + c / 32;
-            s_a[tt][pc] = expf(gate_log_decay(s_eA[c], to_f32(z[idx])));
+            // alpha = exp(g): g from the bounded gate, or given directly (any value)
+            s_a[tt][pc] = expf(g_direct ? g_direct[idx] : gate_log_decay(s_eA[c], to_f32(z[idx])));
             s_k[tt][pc] = to_f32(k[idx]);
             s_q[tt][pc] = to_f32(q[idx]);
         }
@@ -349,13 +351,13 @@ static cudaError_t serial_dispatch(const void *q, const void *k, const void *v, 
                                    const float *A, const float *beta, const int32_t *cu,
                                    int num_seqs, int64_t total, int H, int dk, int dv,
                                    const float *s0, float *s1, void *out, uint32_t *status,
-                                   cudaStream_t st) {
+                                   const float *g, cudaStream_t st) {
     dim3 grid((unsigned)num_seqs * (unsigned)H, (unsigned)(dv / 32));
 #define KDA_SERIAL_CASE(DK_)                                                                   \
     if (dk == DK_) {                                                                           \
         prefill_serial_kernel<T, DK_><<<grid, 128, 0, st>>>(                                   \
             (const T *)q, (const T *)k, (const T *)v, (const T *)z, A, beta, cu, total, H, dv, \
-            s0, s1, (T *)out, status);                                                         \
+            s0, s1, (T *)out, status, g);                                                      \
         return cudaGetLastError();                                                             \
     }
     KDA_SERIAL_CASE(32) KDA_SERIAL_CASE(64) KDA_SERIAL_CASE(128)
@@ -367,12 +369,12 @@ cudaError_t launch_prefill_serial(const void *q, const void *k, const void *v, c
                                   const float *A, const float *beta, const int32_t *cu,
                                   int num_seqs, int64_t total, int H, int dk, int dv, bool bf16,
                                   const float *s0, float *s1, void *out, uint32_t *status,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, const float *g) {
     if ((int64_t)num_seqs * H == 0) return cudaSuccess;
     return bf16 ? serial_dispatch<__nv_bfloat16>(q, k, v, z, A, beta, cu, num_seqs, total, H, dk,
-                                                 dv, s0, s1, out, status, st)
+                                                 dv, s0, s1, out, status, g, st)
                 : serial_dispatch<float>(q, k, v, z, A, beta, cu, num_seqs, total, H, dk, dv, s0,
-                                         s1, out, status, st);
+                                         s1, out, status, g, st);
 }
 
 cudaError_t launch_schedule(const int32_t *cu, int num_seqs, int32_t *order, uint32_t *counter,

@@ -54,6 +54,9 @@ def lib():
             L.kda_chunk_prefill.restype = I
             L.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P]
             L.kda_decode_step.restype = I
+            L.kda_chunk_prefill_logdecay.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, P, P,
+                                                     P, P, SZ, P]
+            L.kda_chunk_prefill_logdecay.restype = I
             L.kda_decode_tokens.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, P, P]
             L.kda_decode_tokens.restype = I
             L.kda_prefill_kernel_launches.argtypes = [I64, I, I, I, I, I, SZ]
@@ -157,6 +160,39 @@ def chunk_prefill(q, k, v, z, A, beta, cu_seqlens, initial_state=None, final_sta
                                  _ptr(initial_state), _ptr(final_state), _ptr(out),
                                  _ptr(workspace), workspace.numel(), _stream(stream))
     _raise(st, "kda_chunk_prefill")
+    return out, final_state
+
+
+def chunk_prefill_logdecay(q, k, v, g, beta, cu_seqlens, initial_state=None, final_state=None,
+                           out=None, workspace=None, want_final_state=True, stream=None):
+    """Prefill with the log-decay g [T, H, dk] f32 given directly (no lower bound);
+    the token-serial kernel.  Other arguments as chunk_prefill."""
+    _check(q, "q")
+    T, H, dk = q.shape
+    dv = v.shape[2] if v.dim() == 3 else -1
+    dev = q.device
+    _check(k, "k", (T, H, dk), q.dtype, dev)
+    _check(v, "v", (T, H, dv), q.dtype, dev)
+    _check(g, "g", (T, H, dk), torch.float32, dev)
+    _check(beta, "beta", (T, H), torch.float32, dev)
+    _check(cu_seqlens, "cu_seqlens", None, torch.int32, dev)
+    N = cu_seqlens.shape[0] - 1
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (N, H, dk, dv), torch.float32, dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check(final_state, "final_state", (N, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _check(out, "out", (T, H, dv), q.dtype, dev)
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=dev)
+    st = lib().kda_chunk_prefill_logdecay(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                          _ptr(cu_seqlens), N, T, H, dk, dv, _dtype_code(q),
+                                          _ptr(initial_state), _ptr(final_state), _ptr(out),
+                                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise(st, "kda_chunk_prefill_logdecay")
     return out, final_state
 
 

@@ -126,6 +126,29 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
                                size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_prefill_logdecay -- the same prefill with the per-channel
+ * log-decay g given directly instead of through the bounded gate, so alpha =
+ * exp(g) with g unbounded below (intended range g <= 0).  "Kimi K3 internals
+ * analysis", section "Sequence mixing": before K3 the log-decay had no lower
+ * bound, the reciprocal cumulative decay of a chunk could overflow, and the
+ * diagonal 16-token tiles needed a special position-pair path instead of the
+ * dense tensor-core one.  This library's chunked tensor-core path relies on
+ * the bound (its right factors e^(R_a - G_s) must stay below the float32
+ * range), so this call runs the token-serial kernel for every dtype and head
+ * size: exact for any decay, and the measure of what the bound buys.
+ *   g          [total_tokens, H, dk] float32 (replaces z and A)
+ *   workspace  at least 4 bytes (the status word), 16-byte aligned
+ * All other arguments as for kda_chunk_prefill.
+ */
+kda_status_t kda_chunk_prefill_logdecay(const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta,
+                                        const int32_t *cu_seqlens, int num_seqs,
+                                        int64_t total_tokens, int H, int dk, int dv,
+                                        kda_dtype_t dtype, const float *initial_state,
+                                        float *final_state, void *out, void *workspace,
+                                        size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_prefill_kernel_launches -- how many kernels one kda_chunk_prefill call
  * with these sizes and this workspace size launches (q, k, v, z and out
  * assumed 16-byte aligned); 0 for an empty batch.  For instrumentation, e.g. a

@@ -64,3 +64,10 @@ def test_host_side_validation(lib):
     # zero-length decode batch
     assert lib.kda_decode_step(None, None, None, None, None, None, None, None, 0, 2, 128, 128,
                                kda.KDA_BF16, None) == kda.KDA_OK
+    # the unbounded-decay prefill: status word needs 4 bytes; dk outside {32, 64, 128}
+    assert lib.kda_chunk_prefill_logdecay(fake, fake, fake, fake, fake, fake, 3, 1000, 2, 128, 128,
+                                          kda.KDA_BF16, None, None, fake, fake, 2,
+                                          None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_prefill_logdecay(fake, fake, fake, fake, fake, fake, 3, 1000, 2, 96, 128,
+                                          kda.KDA_BF16, None, None, fake, fake, 256,
+                                          None) == kda.KDA_ERR_UNSUPPORTED
