@@ -1595,23 +1595,54 @@ prefill_seg_kernel(const SplitParams p) {
 }
 
 // The scan: per chain, S_in(g + 1) = M_g S_in(g) + S0_g for the segments g
-// before the last non-empty one, as one MMA each,
-//   S_in(g+1)^T = S0_g^T + S_in(g)^T M_g^T   (A = S_in^T bf16, B = M_g [c'][c] bf16).
-constexpr uint32_t SC_ST = 0, SC_MB = 32768, SC_BAR = 98304;   // M tiles: two buffers of 32 KB
+// before the last non-empty one.  The value channels (columns j of S) do not
+// mix, so each chain is split over SCAN_SPLIT CTAs of SCAN_JB columns: one CTA
+// keeps S_in[:, j0 .. j0 + 31] and runs, per segment, one M = 128, N = 32 MMA
+//   D[c][j] = S0_g[c][j] + sum_c' M_g[c][c'] S_in(g)[c'][j]
+// (A = M_g as written by the segment kernel, B = the bf16 block S_in^T[j][c']).
+// Thread c owns row c (TMEM lane c).  The 128 x 32 float32 blocks of S0 (two
+// segments ahead) and of S_in move as single TMA tiles (128-byte swizzle), so
+// only the MMA and the bf16 copy of its result are on the chain of a step.
+constexpr int SCAN_JB = 32, SCAN_SPLIT = D / SCAN_JB, SCAN_NT = 128;
+constexpr uint32_t SCAN_BLK = 128 * SCAN_JB * 4;     // bytes of one float32 block
+constexpr int SEG_CELL_ROWS = (int)(SEG_CELL / (D * 4));   // 512-byte rows per (chain, segment) cell
+constexpr uint32_t SC_MB = 0, SC_SB = 65536;         // M tiles: two buffers of 32 KB; B tile 8 KB
+constexpr uint32_t SC_S0 = SC_SB + 8192;             // two S0 blocks
+constexpr uint32_t SC_OUT = SC_S0 + 2 * SCAN_BLK;    // S_in block going out (and the start's transpose)
+constexpr uint32_t SC_BAR = SC_OUT + SCAN_BLK;
 constexpr uint32_t SMEM_SCAN = SC_BAR + 64 + 1024;
+static_assert(SC_S0 % 1024 == 0 && SC_OUT % 1024 == 0 && SEG_CELL % (D * 4) == 0, "scan layout");
 
-__global__ void __launch_bounds__(NT, 1)
-prefill_scan_kernel(const SplitParams p) {
+// Byte offset of element (row r, column j) of a 128 x 32 float32 block in the
+// 128-byte-swizzled TMA layout.
+__device__ __forceinline__ uint32_t scan_off(int r, int j) {
+    return swz(r, j >> 2) + (uint32_t)(j & 3) * 4u;
+}
+
+// This thread's row c of an f32 [c][j] state block into the bf16 B tile S^T[j][c]
+// (32 rows j, K = c in two 64-element blocks of 4 KB).
+__device__ __forceinline__ void scan_block_to_bf16(uint8_t *tile, int c, const float *X) {
+    uint8_t *kb = tile + (c >> 6) * 4096;
+    const uint32_t cc = (uint32_t)((c & 63) >> 3), co = (uint32_t)(c & 7) * 2u;
+#pragma unroll
+    for (int j = 0; j < SCAN_JB; ++j)
+        *reinterpret_cast<__nv_bfloat16 *>(kb + swz(j, cc) + co) = __float2bfloat16_rn(X[j]);
+}
+
+__global__ void __launch_bounds__(SCAN_NT, 1)
+prefill_scan_kernel(const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_sin,
+                    const SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(sm);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + SC_BAR);   // MMA done
     uint64_t *bar_mb = bar + 1;                                  // [2] M tile arrived
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SC_BAR + 24);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + SC_BAR + 32);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int chain = blockIdx.x;
+    uint64_t *bar_s0 = bar + 3;                                  // [2] S0 block arrived
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SC_BAR + 48);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + SC_BAR + 56);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chain = blockIdx.x / SCAN_SPLIT, j0 = (blockIdx.x % SCAN_SPLIT) * SCAN_JB;
     const int seq = chain / p.H;
     int64_t bos = p.cu_seqlens[seq], eos = p.cu_seqlens[seq + 1];
     if (bos < 0 || eos < bos || eos > p.total_tokens) bos = eos = 0;
@@ -1620,80 +1651,138 @@ prefill_scan_kernel(const SplitParams p) {
     if (nseg <= 1) return;   // only the first segment runs, from the initial state
 
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) ptx::mbar_init(bar + i, 1);
+        for (int i = 0; i < 5; ++i) ptx::mbar_init(bar + i, 1);
         ptx::fence_mbar_init();
         *s_abort = 0;
+        ptx::prefetch_tensormap(&tm_s0);
+        ptx::prefetch_tensormap(&tm_sin);
     }
     if (warp == 0) {
-        ptx::tmem_alloc(s_tmem, 128);
+        ptx::tmem_alloc(s_tmem, 2 * SCAN_JB);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
-    const Ctx x = make_ctx(sm, tmem);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const int c = tid;               // row of S (TMEM lane)
     ptx::pdl_wait();                 // the segment maps
     ptx::pdl_launch_dependents();
-    const int64_t sidx = (int64_t)chain * D * D;
-    const uint8_t *cells = p.seg_out + (size_t)chain * p.segs * SEG_CELL;
+    const int cell0 = chain * p.segs;   // this chain's first (chain, segment) cell
+    const uint8_t *cells = p.seg_out + (size_t)cell0 * SEG_CELL;
     uint32_t issued = 0, done = 0, mb_issued[2] = {0, 0}, mb_done[2] = {0, 0};
+    uint32_t s0_issued[2] = {0, 0}, s0_done[2] = {0, 0};
+    auto issue_s0 = [&](int g, int b) {   // S0_g block into staging buffer b
+        if (tid == 0) {
+            ptx::mbar_arrive_expect_tx(bar_s0 + b, SCAN_BLK);
+            ptx::tma_load_2d(sm + SC_S0 + b * SCAN_BLK, &tm_s0, j0, (cell0 + g) * SEG_CELL_ROWS, bar_s0 + b);
+        }
+        ++s0_issued[b];
+    };
+    auto read_row = [&](uint32_t off, float (&Y)[SCAN_JB]) {   // row c of a swizzled block
+#pragma unroll
+        for (int i = 0; i < SCAN_JB / 4; ++i) {
+            const float4 v = *reinterpret_cast<const float4 *>(sm + off + swz(c, i));
+            Y[4 * i] = v.x; Y[4 * i + 1] = v.y; Y[4 * i + 2] = v.z; Y[4 * i + 3] = v.w;
+        }
+    };
+    auto save = [&](int g, uint32_t buf, float (&Y)[SCAN_JB]) {   // S_in(g) block out of TMEM buffer buf
+        ptx::tmem_ld32(lane_base + buf, Y);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < SCAN_JB / 4; ++i)
+            *reinterpret_cast<float4 *>(sm + SC_OUT + swz(c, i)) =
+                make_float4(Y[4 * i], Y[4 * i + 1], Y[4 * i + 2], Y[4 * i + 3]);
+        ptx::fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::tma_store_2d(&tm_sin, j0, (cell0 + g) * D, sm + SC_OUT);
+            ptx::bulk_commit();
+        }
+    };
     if (tid == 0) {
         for (int k = 0; k < 2 && k + 1 < nseg; ++k)
             bulk_load(sm + SC_MB + k * 32768, cells + (size_t)k * SEG_CELL + SEG_MT, 32768, bar_mb + k);
     }
     for (int k = 0; k < 2 && k + 1 < nseg; ++k) ++mb_issued[k];
-    // S_in(0)^T as the bf16 operand (its TMEM copy is overwritten below)
-    load_state(x, p.initial_state ? p.initial_state + sidx : nullptr, 0, SC_ST);
-    // this thread's share of S0_g^T (column 32 cg + i of lane ch), one step ahead
-    float s0r[32];
-    auto fetch = [&](int g) {
-        const float *s0 = reinterpret_cast<const float *>(cells + (size_t)g * SEG_CELL + SEG_S0);
+    for (int k = 0; k < 2 && k + 1 < nseg; ++k) issue_s0(k, k);
+    float X[SCAN_JB];
+    {   // S_in(0): the initial state (or zeros) as the first B operand; warp w loads
+        // rows 32w .. 32w + 31 a row per instruction, turned through the out tile
+        const float *src = p.initial_state ? p.initial_state + (int64_t)chain * D * D +
+                                                 (int64_t)(32 * warp) * D + j0 + lane
+                                           : nullptr;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s0r[i] = s0[(int64_t)(32 * x.cg + i) * D + x.ch];
-    };
-    fetch(0);
+        for (int i = 0; i < SCAN_JB; ++i) X[i] = src ? src[(int64_t)i * D] : 0.f;   // all loads in flight at once
+#pragma unroll
+        for (int i = 0; i < SCAN_JB; ++i) *reinterpret_cast<float *>(sm + SC_OUT + scan_off(32 * warp + i, lane)) = X[i];
+        __syncwarp();
+        read_row(SC_OUT, X);
+        scan_block_to_bf16(sm + SC_SB, c, X);
+    }
+    if (ptx::mbar_wait(bar_s0, s0_done[0] & 1, kWaitBudget)) ++s0_done[0]; else *s_abort = 1;
+    read_row(SC_S0, X);
+    ptx::tmem_st32(lane_base, X);   // accumulator 0 = S0_0 block
+    ptx::tmem_st_wait();
+    // Step g accumulates S_in(g + 1) in TMEM buffer g & 1 (32 columns each);
+    // writing S_in(g) out and staging S0_(g+1) into the other buffer overlap it.
     for (int g = 0; g + 1 < nseg; ++g) {
         const int k = g & 1;
-        ptx::tmem_st32(x.lane_base + 32 * x.cg, s0r);   // D = S0_g^T
-        ptx::tmem_st_wait();
+        const uint32_t dk = (uint32_t)(SCAN_JB * k), dn = (uint32_t)(SCAN_JB * (k ^ 1));
+        if (tid == 0) ptx::bulk_wait_read();   // the last S_in block has left the out tile
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
-        __syncthreads();
+        __syncthreads();   // also: S0 block k has been read by every thread
+        if (*s_abort) break;
         if (tid == 0) {
             if (ptx::mbar_wait(bar_mb + k, mb_done[k] & 1, kWaitBudget)) ++mb_done[k]; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            // D += S_in(g)^T M_g^T  (B = M_g [c'][c])
-            mma_k<8>(tmem, sbase + SC_ST, 16384u, sbase + SC_MB + k * 32768, 16384u,
-                     ptx::idesc_bf16_f32(128, 128), true);
+            mma_k<8>(tmem + dk, sbase + SC_MB + k * 32768, 16384u, sbase + SC_SB, 4096u,
+                     ptx::idesc_bf16_f32(128, SCAN_JB), true);
             ptx::mma_commit(bar);
         }
         ++issued;
-        if (g + 2 < nseg) fetch(g + 1);
+        if (g + 2 < nseg - 1) issue_s0(g + 2, k);
+        ptx::tc_fence_after_sync();
+        if (g >= 1) save(g, dn, X);   // S_in(g), from the last step
+        if (g + 2 < nseg) {           // the other buffer = S0_(g+1) block
+            if (ptx::mbar_wait(bar_s0 + (k ^ 1), s0_done[k ^ 1] & 1, kWaitBudget)) ++s0_done[k ^ 1];
+            else *s_abort = 1;
+            read_row(SC_S0 + (k ^ 1) * SCAN_BLK, X);
+            ptx::tmem_st32(lane_base + dn, X);
+            ptx::tmem_st_wait();
+        }
         if (ptx::mbar_wait(bar, done & 1, kWaitBudget)) ++done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
-        __syncthreads();
-        if (*s_abort) break;
         // this M buffer is free again: fetch the tile two steps ahead into it
         if (tid == 0 && g + 3 < nseg)
             bulk_load(sm + SC_MB + k * 32768, cells + (size_t)(g + 2) * SEG_CELL + SEG_MT, 32768, bar_mb + k);
         if (g + 3 < nseg) ++mb_issued[k];
-        // S_in(g + 1): to the workspace, and as the next operand
-        save_state(x, p.seg_in + ((size_t)chain * p.segs + g + 1) * D * D, 0);
-        state_to_bf16(x, 0, SC_ST);
+        ptx::tmem_ld32(lane_base + dk, X);   // S_in(g + 1): the next step's operand
+        ptx::tmem_ld_wait();
+        scan_block_to_bf16(sm + SC_SB, c, X);
     }
+    if (tid == 0) ptx::bulk_wait_read();
+    ptx::tc_fence_before_sync();
     __syncthreads();
-    if (*s_abort) {
+    if (!*s_abort) {
+        ptx::tc_fence_after_sync();
+        save(nseg - 1, (uint32_t)(SCAN_JB * ((nseg - 2) & 1)), X);
+    } else {
         if (tid == 0) report_status(p.status, kDevTimeout);
         while (done < issued && ptx::mbar_wait(bar, done & 1, kWaitBudget)) ++done;
-        for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < 2; ++k) {
             while (mb_done[k] < mb_issued[k] && ptx::mbar_wait(bar_mb + k, mb_done[k] & 1, kWaitBudget)) ++mb_done[k];
+            while (s0_done[k] < s0_issued[k] && ptx::mbar_wait(bar_s0 + k, s0_done[k] & 1, kWaitBudget)) ++s0_done[k];
+        }
     }
+    if (tid == 0) ptx::bulk_wait_all();   // the S_in blocks are out before the CTA ends
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem, 128);
+        ptx::tmem_dealloc(tmem, 2 * SCAN_JB);
     }
 }
 
@@ -1718,6 +1807,21 @@ static EncodeTiledFn get_encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(ptr);
     }
     return fn;
+}
+
+// A float32 [rows][128] buffer as a 2-D tensor with 32 x 128 boxes (128-byte
+// swizzle): the scan's state blocks.
+static bool make_map_state(CUtensorMap *m, const void *base, int64_t rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)tc::D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)tc::D * 4};
+    cuuint32_t box[2] = {(cuuint32_t)tc::SCAN_JB, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // [T, H*128] bf16 viewed as a 2-D tensor; 64 x 64 boxes, 128-byte swizzle,
@@ -1865,11 +1969,11 @@ cudaError_t launch_schedule(const int32_t *cu, int num_seqs, int32_t *order, uin
 // while the previous kernel of the stream finishes and waits for that
 // kernel's results in ptx::pdl_wait().
 template <typename... KArgs, typename... Args>
-static cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned smem,
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, unsigned smem,
                               cudaStream_t st, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(tc::NT);
+    cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1922,14 +2026,19 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
         const int64_t items = chains * scan.max_chunks;
         if ((e = launch_pdl(tc::prefill_intra_kernel, (unsigned)(items < sms ? items : sms),
-                            tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
+                            tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
             return e;
         sp.segs = scan.segs;
         const unsigned cells = (unsigned)(chains * scan.segs);
-        if ((e = launch_pdl(tc::prefill_seg_kernel, cells, tc::SMEM_SEG, st, sp)) != cudaSuccess) return e;
-        if ((e = launch_pdl(tc::prefill_scan_kernel, (unsigned)chains, tc::SMEM_SCAN, st, sp)) != cudaSuccess)
+        if ((e = launch_pdl(tc::prefill_seg_kernel, cells, tc::NT, tc::SMEM_SEG, st, sp)) != cudaSuccess) return e;
+        CUtensorMap ms0, msin;
+        if (!make_map_state(&ms0, sp.seg_out, chains * scan.segs * tc::SEG_CELL_ROWS) ||
+            !make_map_state(&msin, sp.seg_in, chains * scan.segs * tc::D))
+            return cudaErrorInvalidValue;
+        if ((e = launch_pdl(tc::prefill_scan_kernel, (unsigned)(chains * tc::SCAN_SPLIT), tc::SCAN_NT,
+                            tc::SMEM_SCAN, st, ms0, msin, sp)) != cudaSuccess)
             return e;
-        return launch_pdl(tc::prefill_state_kernel, cells, tc::SMEM_STATE, st, mo, sp);
+        return launch_pdl(tc::prefill_state_kernel, cells, tc::NT, tc::SMEM_STATE, st, mo, sp);
     }
 
     const SplitPlan plan = plan_split(total, num_seqs, H);
@@ -1985,7 +2094,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
     prm.counter = counter; prm.status = status; prm.total_tokens = total;
     prm.num_seqs = num_seqs; prm.H = H;
-    return launch_pdl(tc::prefill_tc_kernel, (unsigned)grid, tc::SMEM_ALLOC, st, mq, mk, mv, mz, mo, prm);
+    return launch_pdl(tc::prefill_tc_kernel, (unsigned)grid, tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, mo, prm);
 }
 
 }  // namespace kda
