@@ -1058,13 +1058,6 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     const Ctx x = make_ctx(sm, tmem);
-    ptx::pdl_wait();                 // the previous kernel's status word (and, windowed, nothing else)
-    ptx::pdl_launch_dependents();
-    // bad sequence offsets are reported once, by the first CTA
-    if (blockIdx.x == 0 && tid < p.num_seqs) {
-        const int64_t b = p.cu_seqlens[tid], e = p.cu_seqlens[tid + 1];
-        if (b < 0 || e < b || e > p.total_tokens) report_status(p.status, kDevBadSeqlens);
-    }
 
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
     uint32_t g_issued = 0, g_done = 0;
@@ -1073,6 +1066,9 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     int it = blockIdx.x;
     while (it < n_items && !item_info(p, it, cur)) it += gridDim.x;
     float ean_cur = 0.f, beta_cur = 0.f;   // this thread's entry of s_eAn / s_beta for the coming item
+    // The inputs were complete before the previous kernel of the call started,
+    // so the first item's tiles are fetched before waiting on that kernel;
+    // nothing is written to global memory before the wait.
     if (it < n_items) {
         if (tid < D) ean_cur = -expf(p.A[cur.h * D + tid]) * kLog2e;
         if (tid < C) beta_cur = (tid < cur.nvalid) ? p.beta[(cur.row0 + tid) * H + cur.h] : 0.f;
@@ -1083,6 +1079,13 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tma_2box(sm + OFF_V, &tm_v, hx, (int)cur.row0, bar_v);
         }
         ++qk_issued; ++z_issued; ++v_issued;
+    }
+    ptx::pdl_wait();                 // the previous kernel's status word (and, windowed, nothing else)
+    ptx::pdl_launch_dependents();
+    // bad sequence offsets are reported once, by the first CTA
+    if (blockIdx.x == 0 && tid < p.num_seqs) {
+        const int64_t b = p.cu_seqlens[tid], e = p.cu_seqlens[tid + 1];
+        if (b < 0 || e < b || e > p.total_tokens) report_status(p.status, kDevBadSeqlens);
     }
     while (it < n_items) {
         int nit = it + gridDim.x;
