@@ -781,7 +781,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         load_state(x, p.initial_state ? p.initial_state + sidx : nullptr, TM_D3, OFF_ST);
         if (tid < D) x.s_eAn[tid] = -expf(p.A[h * D + tid]) * kLog2e;
         float beta_next = 0.f;
-        if (tid < C && nchunks > 0) beta_next = (bos + tid < eos) ? p.beta[(bos + tid) * H + h] : 0.f;
+        if (tid < C && bos + tid < eos) beta_next = p.beta[(bos + tid) * H + h];
         __syncthreads();   // s_eAn visible
 
         for (int cidx = 0; cidx < nchunks; ++cidx) {
@@ -844,8 +844,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ptx::mma_commit(bar_m);
             }
             ++m_issued;
-            if (tid < C && has_next)
-                beta_next = (next_row + tid < eos) ? p.beta[(next_row + tid) * H + h] : 0.f;
+            // (loaded into the register untouched: the load latency hides behind phases C-D)
+            if (tid < C && has_next) {
+                beta_next = 0.f;
+                if (next_row + tid < eos) beta_next = p.beta[(next_row + tid) * H + h];
+            }
 
             // =============================== phase C: U^T to smem, output and state MMAs
             if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
@@ -1065,13 +1068,15 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     ItemInfo cur, nxt;
     int it = blockIdx.x;
     while (it < n_items && !item_info(p, it, cur)) it += gridDim.x;
-    float ean_cur = 0.f, beta_cur = 0.f;   // this thread's entry of s_eAn / s_beta for the coming item
+    // this thread's entry of A and beta for the coming item, raw: loaded one item
+    // ahead and not used until that item starts, so the load latency is hidden
+    float a_cur = 0.f, beta_cur = 0.f;
     // The inputs were complete before the previous kernel of the call started,
     // so the first item's tiles are fetched before waiting on that kernel;
     // nothing is written to global memory before the wait.
     if (it < n_items) {
-        if (tid < D) ean_cur = -expf(p.A[cur.h * D + tid]) * kLog2e;
-        if (tid < C) beta_cur = (tid < cur.nvalid) ? p.beta[(cur.row0 + tid) * H + cur.h] : 0.f;
+        if (tid < D) a_cur = p.A[cur.h * D + tid];
+        if (tid < cur.nvalid) beta_cur = p.beta[(cur.row0 + tid) * H + cur.h];
         if (tid == 0) {
             const int hx = cur.h * D;
             tma_qk(sm, &tm_q, &tm_k, hx, (int)cur.row0, bar_qk);
@@ -1095,15 +1100,16 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int nvalid = cur.nvalid;
         uint8_t *rec = p.records + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * REC_BYTES;
 
-        if (tid < D) x.s_eAn[tid] = ean_cur;
+        if (tid < D) x.s_eAn[tid] = -expf(a_cur) * kLog2e;
         if (tid < C) x.s_beta[tid] = beta_cur;
         // every export but the previous item's last group (-W, U~^T) has left smem
         if (tid == 0) ptx::bulk_wait_read_but1();
         __syncthreads();
         // the next item's gate constants and beta, loaded while this one runs
         if (has_next) {
-            if (tid < D) ean_cur = -expf(p.A[nxt.h * D + tid]) * kLog2e;
-            if (tid < C) beta_cur = (tid < nxt.nvalid) ? p.beta[(nxt.row0 + tid) * H + nxt.h] : 0.f;
+            if (tid < D) a_cur = p.A[nxt.h * D + tid];
+            beta_cur = 0.f;
+            if (tid < nxt.nvalid) beta_cur = p.beta[(nxt.row0 + tid) * H + nxt.h];
         }
 
         phase_gate_operands<true>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
