@@ -24,6 +24,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               void *out, void *workspace, size_t workspace_bytes, cudaStream_t st);
 size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H);
 int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes);
+cudaError_t launch_state_slots(float *pool, int pool_size, const int32_t *slots, float *states,
+                               int N, int H, int dk, int dv, bool to_pool, uint32_t *status,
+                               cudaStream_t st);
 cudaError_t launch_decode_tokens(const void *q, const void *k, const void *v, const void *z,
                                  const float *A, const float *beta, float *pool, int pool_size,
                                  const int32_t *slots, void *out, int N, int n_tok, int H, int dk,
@@ -186,6 +189,19 @@ kda_status_t kda_decode_tokens(const void *q, const void *k, const void *v, cons
     return from_cuda(kda::launch_decode_tokens(q, k, v, z, A, beta, state_pool, pool_size, slot_ids,
                                                out, N, n_tokens, H, dk, dv, dtype == KDA_BF16,
                                                status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status_t kda_state_slots_copy(float *state_pool, int pool_size, const int32_t *slot_ids,
+                                  float *states, int N, int H, int dk, int dv, int to_pool,
+                                  uint32_t *status, kda_stream_t stream) {
+    if (N < 0 || pool_size < 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    if (!state_pool || !slot_ids || !states) return KDA_ERR_INVALID_ARG;
+    if (!aligned(state_pool, 16) || !aligned(states, 16)) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_state_slots(state_pool, pool_size, slot_ids, states, N, H, dk, dv,
+                                             to_pool != 0, status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kda_status_t kda_check_device_status(const void *workspace, kda_stream_t stream) {

@@ -156,6 +156,44 @@ static cudaError_t tokens_dispatch(const void *q, const void *k, const void *v, 
     return cudaErrorInvalidValue;
 }
 
+// Prefill -> decode handoff: N contiguous states [N, H, dk, dv] to or from
+// their pool slots.  One CTA per (row, head), float4 copies; a negative slot
+// skips the row (on a gather its states are zeroed), a slot >= pool_size is
+// reported in *status and treated the same way.
+__global__ void __launch_bounds__(256) state_slots_kernel(float *__restrict__ pool, int pool_size,
+                                                          const int32_t *__restrict__ slots,
+                                                          float *__restrict__ states, int H,
+                                                          int64_t per_head, bool to_pool,
+                                                          uint32_t *status) {
+    const int i = blockIdx.x, h = blockIdx.y;
+    int slot = slots[i];
+    if (slot >= pool_size) {
+        if (threadIdx.x == 0 && h == 0) report_status(status, KDA_ERR_INVALID_ARG);
+        slot = -1;
+    }
+    float4 *row = reinterpret_cast<float4 *>(states + ((int64_t)i * H + h) * per_head);
+    const int64_t n4 = per_head / 4;
+    if (slot < 0) {
+        if (!to_pool)
+            for (int64_t e = threadIdx.x; e < n4; e += blockDim.x) row[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    float4 *cell = reinterpret_cast<float4 *>(pool + ((int64_t)slot * H + h) * per_head);
+    if (to_pool)
+        for (int64_t e = threadIdx.x; e < n4; e += blockDim.x) cell[e] = row[e];
+    else
+        for (int64_t e = threadIdx.x; e < n4; e += blockDim.x) row[e] = cell[e];
+}
+
+cudaError_t launch_state_slots(float *pool, int pool_size, const int32_t *slots, float *states,
+                               int N, int H, int dk, int dv, bool to_pool, uint32_t *status,
+                               cudaStream_t st) {
+    if ((int64_t)N * H == 0) return cudaSuccess;
+    state_slots_kernel<<<dim3((unsigned)N, (unsigned)H), 256, 0, st>>>(
+        pool, pool_size, slots, states, H, (int64_t)dk * dv, to_pool, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode_tokens(const void *q, const void *k, const void *v, const void *z,
                                  const float *A, const float *beta, float *pool, int pool_size,
                                  const int32_t *slots, void *out, int N, int n_tok, int H, int dk,

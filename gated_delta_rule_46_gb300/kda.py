@@ -57,6 +57,8 @@ def lib():
             L.kda_chunk_prefill_logdecay.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, P, P,
                                                      P, P, SZ, P]
             L.kda_chunk_prefill_logdecay.restype = I
+            L.kda_state_slots_copy.argtypes = [P, I, P, P, I, I, I, I, I, P, P]
+            L.kda_state_slots_copy.restype = I
             L.kda_decode_tokens.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, P, P]
             L.kda_decode_tokens.restype = I
             L.kda_prefill_kernel_launches.argtypes = [I64, I, I, I, I, I, SZ]
@@ -227,6 +229,23 @@ def decode_tokens(q, k, v, z, A, beta, state_pool, slot_ids=None, out=None, stat
                                  N, n, H, dk, dv, _dtype_code(q), _ptr(status), _stream(stream))
     _raise(st, "kda_decode_tokens")
     return out
+
+
+def state_slots_copy(state_pool, slot_ids, states, to_pool=True, status=None, stream=None):
+    """Copy states [N, H, dk, dv] f32 into (to_pool) or out of the pool slots
+    slot_ids [N] int32 of state_pool [P, H, dk, dv] f32 (the prefill -> decode
+    handoff).  Returns states."""
+    _check(state_pool, "state_pool")
+    P, H, dk, dv = state_pool.shape
+    dev = state_pool.device
+    _check(state_pool, "state_pool", (P, H, dk, dv), torch.float32, dev)
+    _check(slot_ids, "slot_ids", None, torch.int32, dev)
+    N = slot_ids.shape[0]
+    _check(states, "states", (N, H, dk, dv), torch.float32, dev)
+    st = lib().kda_state_slots_copy(_ptr(state_pool), P, _ptr(slot_ids), _ptr(states), N, H, dk, dv,
+                                    1 if to_pool else 0, _ptr(status), _stream(stream))
+    _raise(st, "kda_state_slots_copy")
+    return states
 
 
 def prefill_kernel_launches(total_tokens, num_seqs, H, dk, dv, dtype, workspace_bytes) -> int:

@@ -241,6 +241,27 @@ kda_status_t kda_decode_tokens(const void *q, const void *k, const void *v, cons
                                uint32_t *status, kda_stream_t stream);
 
 /*
+ * kda_state_slots_copy -- the prefill -> decode handoff of a serving engine:
+ * moves N recurrent states between a contiguous buffer (the final_state or
+ * initial_state of kda_chunk_prefill) and their slots of a decode state pool
+ * (kda_decode_tokens).  "Kimi K3 internals analysis", section "Sequence
+ * mixing": the fixed-size state is what a sequence carries from prefill into
+ * decode.
+ *   state_pool  [pool_size, H, dk, dv] float32, 16-byte aligned
+ *   slot_ids    [N] int32, device.  A negative id skips the row (when copying
+ *               from the pool its states are written as zeros); an id >=
+ *               pool_size is recorded in *status (KDA_ERR_INVALID_ARG) and
+ *               skipped the same way.
+ *   states      [N, H, dk, dv] float32, 16-byte aligned
+ *   to_pool     nonzero: states -> pool slots; zero: pool slots -> states
+ *   status      device uint32 or NULL, as for kda_decode_tokens
+ * Supported: dk, dv in {32, 64, 128}.  Asynchronous on `stream`.
+ */
+kda_status_t kda_state_slots_copy(float *state_pool, int pool_size, const int32_t *slot_ids,
+                                  float *states, int N, int H, int dk, int dv, int to_pool,
+                                  uint32_t *status, kda_stream_t stream);
+
+/*
  * kda_check_device_status -- synchronises `stream`, reads the status word that
  * kda_chunk_prefill keeps in `workspace`, and returns KDA_OK or the recorded
  * device-side error (KDA_ERR_DEVICE_TIMEOUT).  Returns KDA_ERR_CUDA if the

@@ -71,3 +71,10 @@ def test_host_side_validation(lib):
     assert lib.kda_chunk_prefill_logdecay(fake, fake, fake, fake, fake, fake, 3, 1000, 2, 96, 128,
                                           kda.KDA_BF16, None, None, fake, fake, 256,
                                           None) == kda.KDA_ERR_UNSUPPORTED
+    # the pool handoff copy: null slot ids, misaligned pool, unsupported head size
+    assert lib.kda_state_slots_copy(fake, 4, None, fake, 2, 2, 128, 128, 1, None,
+                                    None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_state_slots_copy(P(4100), 4, fake, fake, 2, 2, 128, 128, 1, None,
+                                    None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_state_slots_copy(fake, 4, fake, fake, 2, 2, 96, 128, 0, None,
+                                    None) == kda.KDA_ERR_UNSUPPORTED

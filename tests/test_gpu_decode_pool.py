@@ -88,3 +88,41 @@ def test_invalid_arguments():
     small = torch.zeros((1, 1, 32, 32), dtype=torch.float32, device=dev)
     with pytest.raises(KDAError):          # no slot ids and a pool smaller than N
         decode_tokens(*g, small)
+
+
+def test_prefill_to_decode_handoff_through_pool():
+    """Prefill N prompts, move the final states into pool slots, then decode n
+    more tokens per sequence from the pool: outputs and states equal the
+    oracle over the whole sequences."""
+    from gated_delta_rule_46_gb300 import chunk_prefill, state_slots_copy
+    dev = need_gpu()
+    lens, n, H, d, P = [70, 1, 130, 64, 9], 4, 2, 128, 11
+    slots = [7, 2, 10, 0, 5]
+    N = len(lens)
+    w = inputs.custom([L + n for L in lens], H=H, dk=d, dv=d, dtype=torch.bfloat16, init="randn0.1", wid=45)
+    f = inputs.prefill_inputs(w)
+    cu = f["cu_seqlens"].tolist()
+    pre = torch.cat([torch.arange(cu[i], cu[i] + lens[i]) for i in range(N)])
+    new = torch.cat([torch.arange(cu[i] + lens[i], cu[i + 1]) for i in range(N)])
+    cu_pre = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    g = {x: f[x].to(dev) for x in ("q", "k", "v", "z", "beta")}
+    A = f["A"].to(dev)
+    _, fin = chunk_prefill(*(g[x][pre.to(dev)].contiguous() for x in ("q", "k", "v", "z")), A,
+                           g["beta"][pre.to(dev)].contiguous(), cu_pre.to(dev), f["initial_state"].to(dev))
+    pool = torch.full((P, H, d, d), 3.0, dtype=torch.float32, device=dev)
+    sl = torch.tensor(slots, dtype=torch.int32, device=dev)
+    state_slots_copy(pool, sl, fin, to_pool=True)
+    shp = lambda t, last: t[new.to(dev)].reshape(N, n, H, last).contiguous()
+    out = decode_tokens(shp(g["q"], d), shp(g["k"], d), shp(g["v"], d), shp(g["z"], d), A,
+                        g["beta"][new.to(dev)].reshape(N, n, H).contiguous(), pool, slot_ids=sl)
+    back = state_slots_copy(pool, torch.tensor([0, -1, 7], dtype=torch.int32, device=dev),
+                            torch.full((3, H, d, d), 5.0, dtype=torch.float32, device=dev), to_pool=False)
+    torch.cuda.synchronize()
+    ro, rf = oracle.prefill(f["q"], f["k"], f["v"], f["z"], f["A"], f["beta"], f["cu_seqlens"], f["initial_state"])
+    assert_close("outputs", out.reshape(-1, H, d), ro[new.numpy()], torch.bfloat16)
+    assert_close("states", pool[sl.long()], rf, torch.bfloat16)
+    for s_ in range(P):
+        if s_ not in slots:
+            assert torch.all(pool[s_] == 3.0), s_          # untouched slots
+    assert torch.equal(back[0], pool[0]) and torch.equal(back[2], pool[7])
+    assert torch.count_nonzero(back[1]) == 0               # padding row zeroed

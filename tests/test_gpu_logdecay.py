@@ -67,3 +67,21 @@ def test_logdecay_invalid_arguments():
     with pytest.raises(KDAError):          # a workspace without room for the status word
         chunk_prefill_logdecay(x["q"], x["k"], x["v"], g, x["beta"], x["cu_seqlens"],
                                workspace=torch.zeros(0, dtype=torch.uint8, device=dev))
+
+
+def test_serial_kernel_few_and_many_chains():
+    """The token-serial kernel on few (sequence, head) chains and on many (one
+    CTA per chain and 32 value channels), against the oracle (float32)."""
+    dev = need_gpu()
+    for lens, H in (([40, 7, 90], 2), ([23] * 96, 4)):   # 24 and 1536 (chain, 32-column) blocks
+        w = inputs.custom(lens, H=H, dk=128, dv=128, dtype=torch.float32, init="randn0.1", wid=64)
+        d = inputs.prefill_inputs(w)
+        g = torch.from_numpy(_unbounded_g(w.total_tokens, w.H, 128, 64))
+        x = to_device(d, dev)
+        out, fin = chunk_prefill_logdecay(x["q"], x["k"], x["v"], g.to(dev), x["beta"], x["cu_seqlens"],
+                                          x["initial_state"])
+        torch.cuda.synchronize()
+        ro, rf = oracle.prefill(d["q"], d["k"], d["v"], None, None, d["beta"], d["cu_seqlens"],
+                                d["initial_state"], g=g.numpy())
+        assert_close("outputs", out, ro, torch.float32)
+        assert_close("states", fin, rf, torch.float32)
