@@ -23,6 +23,11 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
                               void *out, void *workspace, size_t workspace_bytes, cudaStream_t st);
 size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H);
+size_t prefill_tc_logdecay_workspace_bytes(int64_t total, int num_seqs, int H);
+cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void *v, const float *g,
+                                       const float *beta, const int32_t *cu, int num_seqs,
+                                       int64_t total, int H, const float *s0, float *s1, void *out,
+                                       void *workspace, size_t workspace_bytes, cudaStream_t st);
 int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes);
 cudaError_t launch_state_slots(float *pool, int pool_size, const int32_t *slots, float *states,
                                int N, int H, int dk, int dv, bool to_pool, uint32_t *status,
@@ -91,6 +96,19 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int num_seqs, int H, int
     return bytes;
 }
 
+size_t kda_prefill_logdecay_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                           kda_dtype_t dtype) {
+    if (num_seqs < 0) num_seqs = 0;
+    size_t bytes = kda::kWsOrder + sizeof(int32_t) * (size_t)num_seqs;
+    bytes = (bytes + 255) & ~size_t(255);
+    if (dtype == KDA_BF16 && dk == 128 && dv == 128 && H > 0 && total_tokens > 0 &&
+        total_tokens < (int64_t(1) << 31)) {
+        const size_t extra = kda::prefill_tc_logdecay_workspace_bytes(total_tokens, num_seqs, H);
+        if (extra > bytes) bytes = (extra + 255) & ~size_t(255);
+    }
+    return bytes;
+}
+
 int kda_prefill_kernel_launches(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
                                 kda_dtype_t dtype, size_t workspace_bytes) {
     if (num_seqs <= 0 || H <= 0) return 0;
@@ -150,6 +168,14 @@ kda_status_t kda_chunk_prefill_logdecay(const void *q, const void *k, const void
     if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the chunked tensor-core path (bf16, 128 x 128 heads, few long chains) when
+    // the workspace holds its plan; the token-serial kernel otherwise
+    if (use_tc(dtype, dk, dv, q, k, v, g, out, total_tokens)) {
+        const cudaError_t e = kda::launch_prefill_tc_logdecay(q, k, v, g, beta, cu_seqlens, num_seqs,
+                                                              total_tokens, H, initial_state, final_state,
+                                                              out, workspace, workspace_bytes, st);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
     uint32_t *status = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + kda::kWsStatus);
     if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return KDA_ERR_CUDA;
     return from_cuda(kda::launch_prefill_serial(q, k, v, nullptr, nullptr, beta, cu_seqlens,

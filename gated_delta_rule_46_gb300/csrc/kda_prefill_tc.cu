@@ -210,7 +210,22 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
 // [Q^; K^] in place over the q/k tiles, the right factors of the four Gram/P
 // tiles, [K~; Q~] and Kend^T, and 2^(G_end).  Waits for the z and q/k tiles
 // itself.
-template <bool KT>
+//
+// UNB: the log-decay g is given directly, unbounded below ("Kimi K3 internals
+// analysis", section "Sequence mixing": the prior design's gate), as float32
+// in four 32-channel TMA boxes (g_box_off).  The tile factorisation then holds only
+// off the diagonal: every factor is formed as one power 2^(e) with e <= 0
+// (left 2^(G_t - R_ta), right 2^(R_a2 - G_t) for a2 > ta, Kend 2^(G_end - G_t)),
+// the diagonal tiles' right factors are zero, and those tiles are added
+// position pair by position pair in the extraction (diag_tiles_kernel).
+// Shared-memory offset of g box b (channels 32 b .. 32 b + 31) in the unbounded
+// mode: the z region, then the K~ halves of B1, which the intra-chunk kernel
+// does not use.
+__device__ __forceinline__ uint32_t g_box_off(int b) {
+    return b < 2 ? OFF_Z + 8192u * (uint32_t)b : OFF_B1 + 16384u * (uint32_t)(b - 2);
+}
+
+template <bool KT, bool UNB = false>
 __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, uint64_t *bar_z,
                                                     uint32_t &z_done, uint64_t *bar_qk,
                                                     uint32_t &qk_done, volatile int *s_abort) {
@@ -232,10 +247,19 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int t = 8 * h + i;
-            const float2 zz = bf2_to_f2(*reinterpret_cast<const uint32_t *>(zt + swz(t, cb) + co));
             const bool ok = t < nvalid;
-            run0 += ok ? kGMin2 * rcp(1.f + ex2(ea.x * zz.x)) : 0.f;
-            run1 += ok ? kGMin2 * rcp(1.f + ex2(ea.y * zz.y)) : 0.f;
+            if (UNB) {
+                // channels c, c + 1 sit in box 2 kb + (lane >> 4), columns 2 (lane & 15), + 1
+                const uint8_t *gb = sm + g_box_off(2 * kb + (lane >> 4));
+                const float2 gg = *reinterpret_cast<const float2 *>(
+                    gb + swz(t, (lane & 15) >> 1) + 8u * (uint32_t)(lane & 1));
+                run0 += ok ? fmaxf(gg.x, -100.f) * kLog2e : 0.f;
+                run1 += ok ? fmaxf(gg.y, -100.f) * kLog2e : 0.f;
+            } else {
+                const float2 zz = bf2_to_f2(*reinterpret_cast<const uint32_t *>(zt + swz(t, cb) + co));
+                run0 += ok ? kGMin2 * rcp(1.f + ex2(ea.x * zz.x)) : 0.f;
+                run1 += ok ? kGMin2 * rcp(1.f + ex2(ea.y * zz.y)) : 0.f;
+            }
             g0[i] = run0;
             g1[i] = run1;
         }
@@ -281,9 +305,9 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
         const uint32_t oq = swz(t, cb) + co, okk = swz(64 + t, cb) + co;
         const float2 qv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qk + oq));
         const float2 kv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qk + okk));
-        const float x0 = hp0 + g0[i], x1 = hp1 + g1[i];   // G_t - R_ta, in (-115.4, 0]
+        const float x0 = hp0 + g0[i], x1 = hp1 + g1[i];   // G_t - R_ta, in (-115.4, 0] when bounded
         const float el0 = ok ? ex2(x0) : 0.f, el1 = ok ? ex2(x1) : 0.f;     // left factors
-        const float dd0 = ok ? ex2(-x0) : 0.f, dd1 = ok ? ex2(-x1) : 0.f;   // right factors
+        const float dd0 = (ok && !UNB) ? ex2(-x0) : 0.f, dd1 = (ok && !UNB) ? ex2(-x1) : 0.f;   // right factors
         const float qe0 = qv.x * el0, qe1 = qv.y * el1, kh0 = kv.x * el0, kh1 = kv.y * el1;
         *reinterpret_cast<uint32_t *>(qk + oq) = pack_bf16(qe0, qe1);        // [Q^; K^] in place
         *reinterpret_cast<uint32_t *>(qk + okk) = pack_bf16(kh0, kh1);
@@ -291,15 +315,28 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
         kt1[i] = kh1 * rho1;
         if (!KT) *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kt0[i], kt1[i]);   // K~ (KT: as K~^T)
         *reinterpret_cast<uint32_t *>(b1 + okk) = pack_bf16(qe0 * rho0, qe1 * rho1);   // Q~
-        const float fr0 = kv.x * dd0, fr1 = kv.y * dd1;                     // k 2^(R_ta - G_t)
-        kr0[i] = fr0 * ke0;                                                 // k 2^(G_end - G_t)
-        kr1[i] = fr1 * ke1;
-        // right factors for the Gram/P tiles a2 >= ta: k 2^(R_a2 - G_t)
+        if (UNB) {
+            // every factor as one power with a non-positive exponent
+            kr0[i] = ok ? kv.x * ex2((R0[4] - Rt0) - x0) : 0.f;             // k 2^(G_end - G_t)
+            kr1[i] = ok ? kv.y * ex2((R1[4] - Rt1) - x1) : 0.f;
 #pragma unroll
-        for (int a2 = 0; a2 < 4; ++a2)
-            if (a2 >= ta)
-                *reinterpret_cast<uint32_t *>(gb + swz(tile_off(a2) + t, cb) + co) =
-                    pack_bf16(fr0 * f0[a2], fr1 * f1[a2]);
+            for (int a2 = 0; a2 < 4; ++a2)
+                if (a2 >= ta) {
+                    const float r0 = (a2 > ta && ok) ? kv.x * ex2((R0[a2] - Rt0) - x0) : 0.f;
+                    const float r1 = (a2 > ta && ok) ? kv.y * ex2((R1[a2] - Rt1) - x1) : 0.f;
+                    *reinterpret_cast<uint32_t *>(gb + swz(tile_off(a2) + t, cb) + co) = pack_bf16(r0, r1);
+                }
+        } else {
+            const float fr0 = kv.x * dd0, fr1 = kv.y * dd1;                 // k 2^(R_ta - G_t)
+            kr0[i] = fr0 * ke0;                                             // k 2^(G_end - G_t)
+            kr1[i] = fr1 * ke1;
+            // right factors for the Gram/P tiles a2 >= ta: k 2^(R_a2 - G_t)
+#pragma unroll
+            for (int a2 = 0; a2 < 4; ++a2)
+                if (a2 >= ta)
+                    *reinterpret_cast<uint32_t *>(gb + swz(tile_off(a2) + t, cb) + co) =
+                        pack_bf16(fr0 * f0[a2], fr1 * f1[a2]);
+        }
     }
     st_chunk(sm + OFF_KE, swz(c, h), kr0);
     st_chunk(sm + OFF_KE, swz(c + 1, h), kr1);
@@ -311,7 +348,11 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
 
 // P (TMEM rows 0..63 of the Gram/P accumulator) and L (rows 64..127), masked
 // to the causal pattern: P into its bf16 operand tile, L (times beta) in float32.
-__device__ __forceinline__ void phase_extract_PL(const Ctx &x, uint32_t off_pb) {
+// diag (optional): the four diagonal 16 x 16 tiles computed position pair by
+// position pair, [L without beta | P][tile][t][s] float32, added where the
+// Gram/P MMA left them zero.
+__device__ __forceinline__ void phase_extract_PL(const Ctx &x, uint32_t off_pb,
+                                                 const float *diag = nullptr) {
     uint8_t *sm = x.sm;
     const int warp = x.warp, lane = x.lane, qw = x.qw, cg = x.cg;
     const uint32_t lane_base = x.lane_base;
@@ -332,11 +373,23 @@ __device__ __forceinline__ void phase_extract_PL(const Ctx &x, uint32_t off_pb) 
         ptx::tmem_ld_wait();
         const bool have = cg <= a;
         const float bt = s_beta[t];
+        float dg[16];
+        if (diag && cg == a) {   // this thread's columns are the row's own tile
+            const float4 *src = reinterpret_cast<const float4 *>(diag + ((isL ? 0 : 4) + a) * 256 + (t & 15) * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v4 = src[i];
+                dg[4 * i] = v4.x; dg[4 * i + 1] = v4.y; dg[4 * i + 2] = v4.z; dg[4 * i + 3] = v4.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dg[i] = 0.f;
+        }
         float vals[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int s = colbase + i;
-            const float d = have ? ((lane < 16) ? X[i] : Y[i]) : 0.f;
+            const float d = (have ? ((lane < 16) ? X[i] : Y[i]) : 0.f) + dg[i];
             vals[i] = isL ? ((s < t) ? bt * d : 0.f) : ((s <= t) ? d : 0.f);
         }
         if (isL) {
@@ -959,7 +1012,13 @@ struct SplitParams {
     uint8_t *seg_out;          // [chains][segs] cells of SEG_CELL bytes: S0 (from a zero state, float32
                                // [c][j]) and M (bf16 tile M[c'][c], the scan's B operand layout)
     float *seg_in;             // [chains][segs][128][128]: the state each segment starts from
+    // unbounded log-decay (kda_chunk_prefill_logdecay): inputs of the diagonal
+    // tiles' pre-pass, and its output per record slot ([L | P][tile][16][16])
+    const __nv_bfloat16 *q, *k;
+    const float *g;
+    float *diag;
 };
+
 
 __device__ __forceinline__ void bulk_store(uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
@@ -1009,6 +1068,71 @@ __device__ __forceinline__ bool item_info(const SplitParams &p, int it, ItemInfo
     return true;
 }
 
+// ---- diagonal tiles for an unbounded log-decay -------------------------------
+// With no bound on g a diagonal 16-token tile cannot be split into bounded left
+// and right factors, so its entries are summed position pair by position pair:
+//   L'_ts = sum_c k_tc k_sc 2^(G_tc - G_sc),  P_ts = sum_c q_tc k_sc 2^(G_tc - G_sc),
+// s <= t in the same tile (L' without beta and only for s < t), with G the
+// tile-local inclusive log2 decay, so every power is <= 1.  One CTA per work
+// item of the window (as in the intra-chunk kernel); rows past the sequence end
+// count as zero keys and queries.
+constexpr int DG_P = 129;   // padded row of the staged tiles
+constexpr uint32_t SMEM_DIAG = 3 * 64 * DG_P * 4;
+
+__global__ void __launch_bounds__(256)
+diag_tiles_kernel(const SplitParams p) {
+    extern __shared__ float dsm[];
+    float *Kt = dsm, *Qt = dsm + 64 * DG_P, *Gt = dsm + 2 * 64 * DG_P;
+    const int tid = threadIdx.x;
+    const int n_items = p.num_seqs * p.H * p.wn;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        ItemInfo cur;
+        if (!item_info(p, it, cur)) continue;   // uniform over the CTA
+        const int64_t rs = (int64_t)p.H * D;     // row stride of q, k, g
+        __syncthreads();                         // the previous item's tiles are consumed
+        for (int e = tid; e < 64 * D; e += 256) {
+            const int t = e >> 7, c = e & (D - 1);
+            const bool ok = t < cur.nvalid;
+            const int64_t gi = (cur.row0 + t) * rs + (int64_t)cur.h * D + c;
+            Kt[t * DG_P + c] = ok ? __bfloat162float(p.k[gi]) : 0.f;
+            Qt[t * DG_P + c] = ok ? __bfloat162float(p.q[gi]) : 0.f;
+            Gt[t * DG_P + c] = ok ? fmaxf(p.g[gi], -100.f) * kLog2e : 0.f;
+        }
+        __syncthreads();
+        for (int e = tid; e < 4 * D; e += 256) {   // tile-local inclusive sums, per (tile, channel)
+            const int a = e >> 7, c = e & (D - 1);
+            float run = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                run += Gt[(16 * a + i) * DG_P + c];
+                Gt[(16 * a + i) * DG_P + c] = run;
+            }
+        }
+        __syncthreads();
+        float *out = p.diag + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * 2048;
+        for (int e = tid; e < 1024; e += 256) {
+            const int a = e >> 8, t = (e >> 4) & 15, s_ = e & 15;
+            float l = 0.f, pp = 0.f;
+            if (s_ <= t) {
+                const float *kt = Kt + (16 * a + t) * DG_P, *qt = Qt + (16 * a + t) * DG_P;
+                const float *ks = Kt + (16 * a + s_) * DG_P;
+                const float *gt = Gt + (16 * a + t) * DG_P, *gs = Gt + (16 * a + s_) * DG_P;
+                if (s_ == t) {
+                    for (int c = 0; c < D; ++c) pp += qt[c] * ks[c];
+                } else {
+                    for (int c = 0; c < D; ++c) {
+                        const float f = ks[c] * ex2(gt[c] - gs[c]);
+                        l += kt[c] * f;
+                        pp += qt[c] * f;
+                    }
+                }
+            }
+            out[e] = l;
+            out[1024 + e] = pp;
+        }
+    }
+}
+
 // W and U~^T out of TMEM into their staging tiles: -W [t][c] as the two 64-row
 // K-block halves of the [-W; Q~] operand (lanes t < 64, 32 columns per
 // thread), U~^T [j][t] (all lanes, 16 columns per thread).
@@ -1030,6 +1154,9 @@ __device__ __forceinline__ void phase_wu_out(const Ctx &x) {
     st_chunk(x.sm + OFF_UT_INTRA, swz(x.ch, 2 * x.cg + 1), Ut + 8);
 }
 
+// UNB: the log-decay is given (tm_z maps g, float32, in 32-channel boxes) and
+// the diagonal tiles come from diag_tiles_kernel; see phase_gate_operands.
+template <bool UNB>
 __global__ void __launch_bounds__(NT, 1)
 prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -1042,13 +1169,16 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint64_t *bar_z = bar_qk + 1;
     uint64_t *bar_v = bar_qk + 2;
     uint64_t *bar_g = bar_qk + 3;      // Gram/P MMA, then W/U~ MMAs done
+    uint64_t *bar_d = bar_qk + 4;      // UNB: the item's diagonal tiles staged
+    // UNB: the diagonal tiles are staged behind P (free until U~^T is staged)
+    constexpr uint32_t OFF_DG = OFF_PB + 8192;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + OFF_SLOT);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 8);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int H = p.H;
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) ptx::mbar_init(bar_qk + i, 1);
+        for (int i = 0; i < 5; ++i) ptx::mbar_init(bar_qk + i, 1);
         ptx::fence_mbar_init();
         *s_abort = 0;
     }
@@ -1063,7 +1193,15 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const Ctx x = make_ctx(sm, tmem);
 
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
-    uint32_t g_issued = 0, g_done = 0;
+    uint32_t g_issued = 0, g_done = 0, d_issued = 0, d_done = 0;
+    auto load_gz = [&](int hx, int row) {   // z tile, or the four g boxes
+        if (UNB) {
+            ptx::mbar_arrive_expect_tx(bar_z, 32768);
+            for (int b = 0; b < 4; ++b) ptx::tma_load_2d(sm + g_box_off(b), &tm_z, hx + 32 * b, row, bar_z);
+        } else {
+            tma_2box(sm + OFF_Z, &tm_z, hx, row, bar_z);
+        }
+    };
     const int n_items = p.num_seqs * H * p.wn;
     ItemInfo cur, nxt;
     int it = blockIdx.x;
@@ -1075,12 +1213,12 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // so the first item's tiles are fetched before waiting on that kernel;
     // nothing is written to global memory before the wait.
     if (it < n_items) {
-        if (tid < D) a_cur = p.A[cur.h * D + tid];
+        if (!UNB && tid < D) a_cur = p.A[cur.h * D + tid];   // (no gate constants for a given g)
         if (tid < cur.nvalid) beta_cur = p.beta[(cur.row0 + tid) * H + cur.h];
         if (tid == 0) {
             const int hx = cur.h * D;
             tma_qk(sm, &tm_q, &tm_k, hx, (int)cur.row0, bar_qk);
-            tma_2box(sm + OFF_Z, &tm_z, hx, (int)cur.row0, bar_z);
+            load_gz(hx, (int)cur.row0);
             tma_2box(sm + OFF_V, &tm_v, hx, (int)cur.row0, bar_v);
         }
         ++qk_issued; ++z_issued; ++v_issued;
@@ -1107,12 +1245,12 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __syncthreads();
         // the next item's gate constants and beta, loaded while this one runs
         if (has_next) {
-            if (tid < D) a_cur = p.A[nxt.h * D + tid];
+            if (!UNB && tid < D) a_cur = p.A[nxt.h * D + tid];
             beta_cur = 0.f;
             if (tid < nxt.nvalid) beta_cur = p.beta[(nxt.row0 + tid) * H + nxt.h];
         }
 
-        phase_gate_operands<true>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
+        phase_gate_operands<true, UNB>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
         if (tid == 0) ptx::bulk_wait_read();   // -W and U~^T staging free for this item
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
@@ -1120,7 +1258,11 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (*s_abort) break;
         if (tid == 0) {
             ptx::tc_fence_after_sync();
-            if (has_next) tma_2box(sm + OFF_Z, &tm_z, nhx, (int)nxt.row0, bar_z);
+            if (has_next) load_gz(nhx, (int)nxt.row0);
+            if (UNB)   // this item's diagonal tiles, into the space behind P
+                bulk_load(sm + OFF_DG, reinterpret_cast<const uint8_t *>(
+                                           p.diag + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * 2048),
+                          8192, bar_d);
             mma_k<8>(tmem + TM_G, sbase + OFF_QK, 16384u, sbase + OFF_GB, GB_KBLK,
                      ptx::idesc_bf16_f32(128, 160), false);
             ptx::mma_commit(bar_g);
@@ -1132,14 +1274,18 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         ++g_issued;
         if (has_next) ++z_issued;
+        if (UNB) ++d_issued;
         if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
         phase_vt(x, nvalid);
 
         if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
         if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, nhx, (int)nxt.row0, bar_qk);
         if (has_next) ++qk_issued;
+        if (UNB) {
+            if (ptx::mbar_wait(bar_d, d_done & 1, kWaitBudget)) ++d_done; else *s_abort = 1;
+        }
         ptx::tc_fence_after_sync();
-        phase_extract_PL(x, OFF_PB);
+        phase_extract_PL(x, OFF_PB, UNB ? reinterpret_cast<const float *>(sm + OFF_DG) : nullptr);
         ptx::fence_async_smem();
         __syncthreads();
         phase_diag(x);
@@ -1191,6 +1337,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         while (z_done < z_issued && ptx::mbar_wait(bar_z, z_done & 1, kWaitBudget)) ++z_done;
         while (v_done < v_issued && ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done;
         while (g_done < g_issued && ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done;
+        while (d_done < d_issued && ptx::mbar_wait(bar_d, d_done & 1, kWaitBudget)) ++d_done;
     }
     if (tid == 0) ptx::bulk_wait_all();
     ptx::tc_fence_before_sync();
@@ -1833,6 +1980,21 @@ static bool make_map_state(CUtensorMap *m, const void *base, int64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The log-decay g, [T, H*128] float32, as a 2-D tensor with 32 x 64 boxes
+// (128-byte rows, 128-byte swizzle); rows beyond T read as zeros.
+static bool make_map_g(CUtensorMap *m, const float *base, int64_t T, int H) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)H * 128, (cuuint64_t)T};
+    cuuint64_t strides[1] = {(cuuint64_t)H * 128 * 4};
+    cuuint32_t box[2] = {32, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [T, H*128] bf16 viewed as a 2-D tensor; 64 x 64 boxes, 128-byte swizzle,
 // rows beyond T read as zeros.
 static bool make_map(CUtensorMap *m, const void *base, int64_t T, int H) {
@@ -1934,6 +2096,15 @@ size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H) {
 
 // Kernels one tensor-core prefill launches: the schedule kernel, then either
 // the fused kernel or an intra and a state kernel per window.
+// The chunked path for a given (unbounded) log-decay: the segment-scan plan
+// plus the diagonal tiles of every chunk; 0 when that plan does not apply.
+size_t prefill_tc_logdecay_workspace_bytes(int64_t total, int num_seqs, int H) {
+    const ScanPlan c = plan_scan(total, num_seqs, H);
+    if (!c.ok) return 0;
+    const size_t diag_off = (c.bytes + 255) & ~size_t(255);
+    return diag_off + (size_t)num_seqs * H * c.max_chunks * 8192;
+}
+
 int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes) {
     const ScanPlan c = plan_scan(total, num_seqs, H);
     if (c.ok && workspace_bytes >= c.bytes) return 5;
@@ -1993,6 +2164,76 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned 
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Prefill with the log-decay g given (any value): schedule, the diagonal
+// tiles' pre-pass, the intra-chunk kernel in its unbounded mode, then the
+// segment maps, the scan and the state pass of the segment-scan plan.  Returns
+// cudaErrorNotSupported when that plan does not apply or the workspace is too
+// small (the caller then runs the token-serial kernel).
+cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void *v, const float *g,
+                                       const float *beta, const int32_t *cu, int num_seqs,
+                                       int64_t total, int H, const float *s0, float *s1, void *out,
+                                       void *workspace, size_t workspace_bytes, cudaStream_t st) {
+    const ScanPlan scan = plan_scan(total, num_seqs, H);
+    const size_t need = prefill_tc_logdecay_workspace_bytes(total, num_seqs, H);
+    if (!scan.ok || need == 0 || workspace_bytes < need) return cudaErrorNotSupported;
+    CUtensorMap mq, mk, mv, mg, mo;
+    if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) ||
+        !make_map(&mv, v, total, H) || !make_map_g(&mg, g, total, H) ||
+        !make_map(&mo, out, total, H))
+        return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws + kWsStatus);
+    uint32_t *counter = reinterpret_cast<uint32_t *>(ws + kWsCounter);
+    int32_t *order = reinterpret_cast<int32_t *>(ws + kWsOrder);
+    cudaError_t e = launch_schedule(cu, num_seqs, order, counter, status, st);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    const int64_t chains = (int64_t)num_seqs * H;
+    const void *kernels[5] = {(const void *)tc::prefill_intra_kernel<true>, (const void *)tc::prefill_seg_kernel,
+                              (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel,
+                              (const void *)tc::diag_tiles_kernel};
+    const uint32_t smem[5] = {tc::SMEM_ALLOC, tc::SMEM_SEG, tc::SMEM_SCAN, tc::SMEM_STATE, tc::SMEM_DIAG};
+    for (int i = 0; i < 5; ++i)
+        if ((e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem[i])) != cudaSuccess)
+            return e;
+    tc::SplitParams sp;
+    sp.A = nullptr; sp.beta = beta; sp.cu_seqlens = cu; sp.initial_state = s0; sp.final_state = s1;
+    sp.out = static_cast<__nv_bfloat16 *>(out);
+    sp.records = ws + scan.rec_off;
+    sp.states = nullptr;
+    sp.status = status; sp.total_tokens = total; sp.num_seqs = num_seqs; sp.H = H;
+    sp.w0 = 0;
+    sp.wn = (int)scan.max_chunks;
+    sp.W = (int)scan.max_chunks;
+    sp.segs = 1;
+    sp.seg_len = scan.seg_len;
+    sp.seg_out = ws + scan.seg_out_off;
+    sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
+    sp.q = static_cast<const __nv_bfloat16 *>(q);
+    sp.k = static_cast<const __nv_bfloat16 *>(k);
+    sp.g = g;
+    sp.diag = reinterpret_cast<float *>(ws + ((scan.bytes + 255) & ~size_t(255)));
+    const int64_t items = chains * scan.max_chunks;
+    // a plain launch: it waits for the schedule (status word) like any kernel
+    tc::diag_tiles_kernel<<<(unsigned)(items < 4 * sms ? items : 4 * sms), 256, tc::SMEM_DIAG, st>>>(sp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(tc::prefill_intra_kernel<true>, (unsigned)(items < sms ? items : sms),
+                        tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mg, sp)) != cudaSuccess)
+        return e;
+    sp.segs = scan.segs;
+    const unsigned cells = (unsigned)(chains * scan.segs);
+    if ((e = launch_pdl(tc::prefill_seg_kernel, cells, tc::NT, tc::SMEM_SEG, st, sp)) != cudaSuccess) return e;
+    CUtensorMap ms0, msin;
+    if (!make_map_state(&ms0, sp.seg_out, chains * scan.segs * tc::SEG_CELL_ROWS) ||
+        !make_map_state(&msin, sp.seg_in, chains * scan.segs * tc::D))
+        return cudaErrorInvalidValue;
+    if ((e = launch_pdl(tc::prefill_scan_kernel, (unsigned)(chains * tc::SCAN_SPLIT), tc::SCAN_NT,
+                        tc::SMEM_SCAN, st, ms0, msin, sp)) != cudaSuccess)
+        return e;
+    return launch_pdl(tc::prefill_state_kernel, cells, tc::NT, tc::SMEM_STATE, st, mo, sp);
+}
+
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
@@ -2013,7 +2254,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
 
     const ScanPlan scan = plan_scan(total, num_seqs, H);
     if (scan.ok && workspace_bytes >= scan.bytes) {
-        const void *kernels[4] = {(const void *)tc::prefill_intra_kernel, (const void *)tc::prefill_seg_kernel,
+        const void *kernels[4] = {(const void *)tc::prefill_intra_kernel<false>, (const void *)tc::prefill_seg_kernel,
                                   (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel};
         const uint32_t smem[4] = {tc::SMEM_ALLOC, tc::SMEM_SEG, tc::SMEM_SCAN, tc::SMEM_STATE};
         for (int i = 0; i < 4; ++i)
@@ -2033,8 +2274,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.seg_len = scan.seg_len;
         sp.seg_out = ws + scan.seg_out_off;
         sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
+        sp.q = nullptr; sp.k = nullptr; sp.g = nullptr; sp.diag = nullptr;
         const int64_t items = chains * scan.max_chunks;
-        if ((e = launch_pdl(tc::prefill_intra_kernel, (unsigned)(items < sms ? items : sms),
+        if ((e = launch_pdl(tc::prefill_intra_kernel<false>, (unsigned)(items < sms ? items : sms),
                             tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
             return e;
         sp.segs = scan.segs;
@@ -2052,7 +2294,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
 
     const SplitPlan plan = plan_split(total, num_seqs, H);
     if (plan.ok && workspace_bytes >= plan.bytes) {
-        e = cudaFuncSetAttribute(tc::prefill_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(tc::prefill_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)tc::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(tc::prefill_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2069,6 +2311,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.status = status; sp.total_tokens = total; sp.num_seqs = num_seqs; sp.H = H;
         sp.W = plan.W;
         sp.segs = 1; sp.seg_len = 0; sp.seg_out = nullptr; sp.seg_in = nullptr;
+        sp.q = nullptr; sp.k = nullptr; sp.g = nullptr; sp.diag = nullptr;
         // fork: the side stream starts after everything already on `st`
         if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
@@ -2083,7 +2326,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             const int64_t items = chains * sp.wn;
             const int64_t cap = wi == 0 ? sms : sms - chains;   // leave room for the state kernel
             const int grid = (int)(items < cap ? items : cap);
-            tc::prefill_intra_kernel<<<grid, tc::NT, tc::SMEM_ALLOC, ss->s>>>(mq, mk, mv, mz, sp);
+            tc::prefill_intra_kernel<false><<<grid, tc::NT, tc::SMEM_ALLOC, ss->s>>>(mq, mk, mv, mz, sp);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             if ((e = cudaEventRecord(ss->intra[buf], ss->s)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(st, ss->intra[buf], 0)) != cudaSuccess) return e;

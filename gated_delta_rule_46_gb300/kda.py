@@ -57,6 +57,8 @@ def lib():
             L.kda_chunk_prefill_logdecay.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, P, P,
                                                      P, P, SZ, P]
             L.kda_chunk_prefill_logdecay.restype = I
+            L.kda_prefill_logdecay_workspace_size.argtypes = [I64, I, I, I, I, I]
+            L.kda_prefill_logdecay_workspace_size.restype = SZ
             L.kda_state_slots_copy.argtypes = [P, I, P, P, I, I, I, I, I, P, P]
             L.kda_state_slots_copy.restype = I
             L.kda_decode_tokens.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, P, P]
@@ -165,6 +167,13 @@ def chunk_prefill(q, k, v, z, A, beta, cu_seqlens, initial_state=None, final_sta
     return out, final_state
 
 
+def logdecay_workspace_size(total_tokens: int, num_seqs: int, H: int, dk: int, dv: int,
+                            dtype=torch.bfloat16) -> int:
+    """Workspace bytes for chunk_prefill_logdecay's chunked path."""
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib().kda_prefill_logdecay_workspace_size(total_tokens, num_seqs, H, dk, dv, code))
+
+
 def chunk_prefill_logdecay(q, k, v, g, beta, cu_seqlens, initial_state=None, final_state=None,
                            out=None, workspace=None, want_final_state=True, stream=None):
     """Prefill with the log-decay g [T, H, dk] f32 given directly (no lower bound);
@@ -189,7 +198,8 @@ def chunk_prefill_logdecay(q, k, v, g, beta, cu_seqlens, initial_state=None, fin
         out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
     _check(out, "out", (T, H, dv), q.dtype, dev)
     if workspace is None:
-        workspace = torch.zeros(256, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(logdecay_workspace_size(T, N, H, dk, dv, q.dtype), dtype=torch.uint8,
+                                device=dev)
     st = lib().kda_chunk_prefill_logdecay(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                           _ptr(cu_seqlens), N, T, H, dk, dv, _dtype_code(q),
                                           _ptr(initial_state), _ptr(final_state), _ptr(out),

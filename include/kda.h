@@ -128,18 +128,29 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
 /*
  * kda_chunk_prefill_logdecay -- the same prefill with the per-channel
  * log-decay g given directly instead of through the bounded gate, so alpha =
- * exp(g) with g unbounded below (intended range g <= 0).  "Kimi K3 internals
+ * exp(g) with g unbounded below (intended range g <= 0; the chunked path takes
+ * values below -100 as -100, where exp(g) is already below the float32 normal
+ * range).  "Kimi K3 internals
  * analysis", section "Sequence mixing": before K3 the log-decay had no lower
  * bound, the reciprocal cumulative decay of a chunk could overflow, and the
  * diagonal 16-token tiles needed a special position-pair path instead of the
- * dense tensor-core one.  This library's chunked tensor-core path relies on
- * the bound (its right factors e^(R_a - G_s) must stay below the float32
- * range), so this call runs the token-serial kernel for every dtype and head
- * size: exact for any decay, and the measure of what the bound buys.
- *   g          [total_tokens, H, dk] float32 (replaces z and A)
- *   workspace  at least 4 bytes (the status word), 16-byte aligned
+ * dense tensor-core one.  That is what this call does for bf16 with dk = dv =
+ * 128 on batches of few long sequences, when the workspace holds
+ * kda_prefill_logdecay_workspace_size() bytes: the diagonal tiles are summed
+ * pair by pair in a pre-pass and every other factor is formed with a
+ * non-positive exponent, then the segment-scan plan runs as for
+ * kda_chunk_prefill.  Otherwise it runs the token-serial kernel (any dtype and
+ * head size; a 4-byte workspace suffices).  Both are exact for any decay; the
+ * measure of what the bound buys.
+ *   g          [total_tokens, H, dk] float32 (replaces z and A), 16-byte aligned
+ *   workspace  16-byte aligned; at least 4 bytes (the status word)
  * All other arguments as for kda_chunk_prefill.
  */
+/* Workspace for kda_chunk_prefill_logdecay's chunked path (the kda_chunk_prefill
+ * minimum when that path does not apply to these sizes). */
+size_t kda_prefill_logdecay_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                           kda_dtype_t dtype);
+
 kda_status_t kda_chunk_prefill_logdecay(const void *q, const void *k, const void *v,
                                         const float *g, const float *beta,
                                         const int32_t *cu_seqlens, int num_seqs,

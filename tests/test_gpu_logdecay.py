@@ -85,3 +85,42 @@ def test_serial_kernel_few_and_many_chains():
                                 d["initial_state"], g=g.numpy())
         assert_close("outputs", out, ro, torch.float32)
         assert_close("states", fin, rf, torch.float32)
+
+
+def test_chunked_unbounded_path_against_oracle():
+    """bf16, 128 x 128 heads, few long sequences: the chunked path (diagonal
+    tiles pair by pair, every other factor with a non-positive exponent) and the
+    token-serial kernel (a 256-byte workspace), both against the oracle."""
+    from gated_delta_rule_46_gb300 import logdecay_workspace_size
+    dev = need_gpu()
+    w = inputs.custom([3000, 1100], H=2, dk=128, dv=128, dtype=torch.bfloat16, init="randn0.1", wid=65)
+    d = inputs.prefill_inputs(w)
+    g = torch.from_numpy(_unbounded_g(w.total_tokens, w.H, 128, 65))
+    x = to_device(d, dev)
+    big = logdecay_workspace_size(w.total_tokens, 2, 2, 128, 128)
+    assert big > 1 << 20                     # the chunked plan applies to this batch
+    ro, rf = oracle.prefill(d["q"], d["k"], d["v"], None, None, d["beta"], d["cu_seqlens"],
+                            d["initial_state"], g=g.numpy())
+    for ws_bytes in (big, 256):
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        out, fin = chunk_prefill_logdecay(x["q"], x["k"], x["v"], g.to(dev), x["beta"], x["cu_seqlens"],
+                                          x["initial_state"], workspace=ws)
+        torch.cuda.synchronize()
+        assert_close(f"outputs ({ws_bytes} B workspace)", out, ro, torch.bfloat16)
+        assert_close(f"states ({ws_bytes} B workspace)", fin, rf, torch.bfloat16)
+
+
+def test_chunked_unbounded_path_on_bounded_gate():
+    """On the bounded gate's own g the chunked unbounded path equals the bounded
+    chunked prefill (same layer, same tolerance)."""
+    dev = need_gpu()
+    w = inputs.custom([4096], H=4, dk=128, dv=128, dtype=torch.bfloat16, init="randn0.1", wid=66)
+    x = to_device(inputs.prefill_inputs(w), dev)
+    g = gate(x["z"], x["A"])
+    ref_out, ref_fin = chunk_prefill(x["q"], x["k"], x["v"], x["z"], x["A"], x["beta"],
+                                     x["cu_seqlens"], x["initial_state"])
+    out, fin = chunk_prefill_logdecay(x["q"], x["k"], x["v"], g, x["beta"], x["cu_seqlens"],
+                                      x["initial_state"])
+    torch.cuda.synchronize()
+    assert_close("outputs", out, ref_out.double().cpu().numpy(), torch.bfloat16)
+    assert_close("states", fin, ref_fin.double().cpu().numpy(), torch.bfloat16)
