@@ -517,11 +517,15 @@ CASES = {
     "long": ("long", 3, None),
     # the fused (many-chain) plan at a size an ncu capture can replay: 1.4 GB
     "fused-16x2048": ("fused-16x2048: 16 seqs x 2048 tokens", [2048] * 16, 32),
+    # the 4096-token workload through kda_chunk_prefill_logdecay (g from the
+    # bounded gate): the chunked path for an unbounded log-decay
+    "prefill-unbounded": ("prefill-unbounded", 1, None),
 }
+UNBOUNDED_CASES = {"prefill-unbounded"}
 
 
 def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, peak, peak_kind,
-                        reps=2, warm=1, lens=None, H=None, name=None):
+                        reps=2, warm=1, lens=None, H=None, name=None, unbounded=False):
     """One KDA layer over a packed batch (by default the varlen or the 1M-token
     workload `wid`): inputs drawn on the device with the same distributions as
     the parity inputs (bf16 q/k L2-normalised, v/z N(0,1), beta = sigmoid(N(0,1)),
@@ -548,11 +552,18 @@ def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, pe
     N = len(lens)
     out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
     fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
-    ws = torch.zeros(kda.workspace_size(T, N, H, d, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    if unbounded:   # the log-decay passed in (here the bounded gate's values)
+        gd = kda.gate(z, A)
+        ws = torch.zeros(kda.logdecay_workspace_size(T, N, H, d, d), dtype=torch.uint8, device=dev)
 
-    def call():
-        kda.chunk_prefill(q, k, v, z, A, beta, cu, None, final_state=fin, out=out, workspace=ws)
+        def call():
+            kda.chunk_prefill_logdecay(q, k, v, gd, beta, cu, None, final_state=fin, out=out, workspace=ws)
+    else:
+        ws = torch.zeros(kda.workspace_size(T, N, H, d, d), dtype=torch.uint8, device=dev)
+
+        def call():
+            kda.chunk_prefill(q, k, v, z, A, beta, cu, None, final_state=fin, out=out, workspace=ws)
 
     for _ in range(warm):
         call()
@@ -614,7 +625,8 @@ def run_case(args):
     kw = {} if isinstance(spec, int) else {"lens": spec, "H": H, "name": name}
     wid = spec if isinstance(spec, int) else 77
     r = _time_large_prefill(kda, inputs, wid, dev, 0, flush, torch.cuda.synchronize,
-                            lambda x: x, peak, peak_kind, reps=args.steps, warm=args.warmup, **kw)
+                            lambda x: x, peak, peak_kind, reps=args.steps, warm=args.warmup,
+                            unbounded=args.case in UNBOUNDED_CASES, **kw)
     r.update({"case": args.case, "steps": args.steps, "warmup": args.warmup,
               "l2": "flushed before every timed call (256 MB write)"})
     print(json.dumps(r))
