@@ -1110,25 +1110,30 @@ diag_tiles_kernel(const SplitParams p) {
         }
         __syncthreads();
         float *out = p.diag + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * 2048;
-        for (int e = tid; e < 1024; e += 256) {
-            const int a = e >> 8, t = (e >> 4) & 15, s_ = e & 15;
+        // the 136 pairs s <= t of each tile, numbered r = t (t + 1) / 2 + s, all
+        // lanes busy; the diagonal (factor 1) through the same expression
+        for (int e = tid; e < 4 * 136; e += 256) {
+            const int a = e / 136, r = e - 136 * a;
+            int t = (int)((sqrtf(8.f * (float)r + 1.f) - 1.f) * 0.5f);
+            while ((t + 1) * (t + 2) / 2 <= r) ++t;
+            while (t * (t + 1) / 2 > r) --t;
+            const int s_ = r - t * (t + 1) / 2;
+            const float *kt = Kt + (16 * a + t) * DG_P, *qt = Qt + (16 * a + t) * DG_P;
+            const float *ks = Kt + (16 * a + s_) * DG_P;
+            const float *gt = Gt + (16 * a + t) * DG_P, *gs = Gt + (16 * a + s_) * DG_P;
             float l = 0.f, pp = 0.f;
-            if (s_ <= t) {
-                const float *kt = Kt + (16 * a + t) * DG_P, *qt = Qt + (16 * a + t) * DG_P;
-                const float *ks = Kt + (16 * a + s_) * DG_P;
-                const float *gt = Gt + (16 * a + t) * DG_P, *gs = Gt + (16 * a + s_) * DG_P;
-                if (s_ == t) {
-                    for (int c = 0; c < D; ++c) pp += qt[c] * ks[c];
-                } else {
-                    for (int c = 0; c < D; ++c) {
-                        const float f = ks[c] * ex2(gt[c] - gs[c]);
-                        l += kt[c] * f;
-                        pp += qt[c] * f;
-                    }
-                }
+#pragma unroll 4
+            for (int c = 0; c < D; ++c) {
+                const float f = ks[c] * ex2(gt[c] - gs[c]);
+                l += kt[c] * f;
+                pp += qt[c] * f;
             }
-            out[e] = l;
-            out[1024 + e] = pp;
+            out[a * 256 + t * 16 + s_] = s_ < t ? l : 0.f;
+            out[1024 + a * 256 + t * 16 + s_] = pp;
+        }
+        for (int e = tid; e < 1024; e += 256) {   // the upper triangles
+            const int t = (e >> 4) & 15, s_ = e & 15;
+            if (s_ > t) { out[e] = 0.f; out[1024 + e] = 0.f; }
         }
     }
 }
