@@ -220,9 +220,12 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
 // position pair by position pair in the extraction (diag_tiles_kernel).
 // Shared-memory offset of g box b (channels 32 b .. 32 b + 31) in the unbounded
 // mode: the z region, then the K~ halves of B1, which the intra-chunk kernel
-// does not use.
+// (KT) does not use, or the V^T tile, which the fused kernel fills only after
+// phase A.
+template <bool KT>
 __device__ __forceinline__ uint32_t g_box_off(int b) {
-    return b < 2 ? OFF_Z + 8192u * (uint32_t)b : OFF_B1 + 16384u * (uint32_t)(b - 2);
+    return b < 2 ? OFF_Z + 8192u * (uint32_t)b
+                 : (KT ? OFF_B1 + 16384u * (uint32_t)(b - 2) : OFF_VT + 8192u * (uint32_t)(b - 2));
 }
 
 template <bool KT, bool UNB = false>
@@ -250,7 +253,7 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
             const bool ok = t < nvalid;
             if (UNB) {
                 // channels c, c + 1 sit in box 2 kb + (lane >> 4), columns 2 (lane & 15), + 1
-                const uint8_t *gb = sm + g_box_off(2 * kb + (lane >> 4));
+                const uint8_t *gb = sm + g_box_off<KT>(2 * kb + (lane >> 4));
                 const float2 gg = *reinterpret_cast<const float2 *>(
                     gb + swz(t, (lane & 15) >> 1) + 8u * (uint32_t)(lane & 1));
                 run0 += ok ? fmaxf(gg.x, -100.f) * kLog2e : 0.f;
@@ -730,6 +733,36 @@ __device__ __forceinline__ void seq_bounds(const int32_t *cu, int seq, int64_t t
     }
 }
 
+__device__ __forceinline__ void bulk_store(uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(ptx::smem_addr(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_copy_in(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
+                                             uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            ptx::smem_addr(sdst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            ptx::smem_addr(sdst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar))
+        : "memory");
+}
+
+// Slot of chunk c of sequence seq (first token bos), head h, in the diagonal-tile
+// store of the unbounded mode (see diag_tiles_kernel).
+__host__ __device__ __forceinline__ int64_t diag_slot(int64_t stride, int h, int64_t bos, int seq, int c) {
+    return (int64_t)h * stride + (bos >> 6) + seq + c;
+}
+
 struct Params {
     const float *A;            // [H, 128]
     const float *beta;         // [T, H]
@@ -743,6 +776,8 @@ struct Params {
     int64_t total_tokens;
     int num_seqs;
     int H;
+    const float *diag;         // unbounded mode: diagonal tiles per chunk (diag_slot)
+    int64_t diag_stride;
 };
 
 __device__ __forceinline__ void tma_qk(uint8_t *sm, const CUtensorMap *tq, const CUtensorMap *tk,
@@ -762,7 +797,10 @@ __device__ __forceinline__ void tma_2box(uint8_t *dst, const CUtensorMap *tm, in
 
 // Fused kernel: one CTA per SM, persistent over (sequence, head) chains taken
 // longest-first; every chunk runs phases A-D above.  Used when the batch has
-// enough chains to fill the GPU.
+// enough chains to fill the GPU.  UNB: the log-decay is given (tm_z maps g as
+// float32 32-channel boxes: two in the z region, two in the V^T tile) and the
+// diagonal tiles come from diag_tiles_kernel; see phase_gate_operands.
+template <bool UNB>
 __global__ void __launch_bounds__(NT, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -777,6 +815,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t *bar_g = bar_qk + 3;      // Gram/P MMA done
     uint64_t *bar_s = bar_qk + 4;      // state MMA done
     uint64_t *bar_m = bar_qk + 5;      // U MMA, then output/state MMAs done
+    uint64_t *bar_d = bar_qk + 6;      // UNB: the chunk's diagonal tiles staged (behind P)
+    constexpr uint32_t OFF_DG = OFF_OST + 8192;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + OFF_SLOT);
     volatile int *s_work = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 4);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 8);
@@ -785,7 +825,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int64_t rowstride = (int64_t)H * D;
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) ptx::mbar_init(bar_qk + i, 1);
+        for (int i = 0; i < 7; ++i) ptx::mbar_init(bar_qk + i, 1);
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
@@ -810,6 +850,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // a barrier's next expected phase parity is (done & 1)
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
     uint32_t g_issued = 0, g_done = 0, s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
+    uint32_t d_issued = 0, d_done = 0;
     const int n_work = p.num_seqs * H;
 
     for (;;) {
@@ -827,12 +868,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
         if (nchunks > 0 && tid == 0) {
             tma_qk(sm, &tm_q, &tm_k, hx, (int)bos, bar_qk);
-            tma_2box(sm + OFF_Z, &tm_z, hx, (int)bos, bar_z);
+            if (UNB) {
+                ptx::mbar_arrive_expect_tx(bar_z, 32768);
+                for (int b = 0; b < 4; ++b)
+                    ptx::tma_load_2d(sm + g_box_off<false>(b), &tm_z, hx + 32 * b, (int)bos, bar_z);
+            } else {
+                tma_2box(sm + OFF_Z, &tm_z, hx, (int)bos, bar_z);
+            }
             tma_2box(sm + OFF_V, &tm_v, hx, (int)bos, bar_v);
         }
         if (nchunks > 0) { ++qk_issued; ++z_issued; ++v_issued; }
         load_state(x, p.initial_state ? p.initial_state + sidx : nullptr, TM_D3, OFF_ST);
-        if (tid < D) x.s_eAn[tid] = -expf(p.A[h * D + tid]) * kLog2e;
+        if (!UNB && tid < D) x.s_eAn[tid] = -expf(p.A[h * D + tid]) * kLog2e;
         float beta_next = 0.f;
         if (tid < C && bos + tid < eos) beta_next = p.beta[(bos + tid) * H + h];
         __syncthreads();   // s_eAn visible
@@ -845,7 +892,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
             // =============================== phase A: gate, cumulative decay, operands
             if (tid < C) x.s_beta[tid] = beta_next;
-            phase_gate_operands<false>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
+            phase_gate_operands<false, UNB>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -853,8 +900,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (tid == 0) {
                 ptx::tc_fence_after_sync();
                 ptx::bulk_wait_read();   // the previous output tile has left OST (P goes there next)
-                // every thread has read its z rows: prefetch the next chunk's
-                if (has_next) tma_2box(sm + OFF_Z, &tm_z, hx, (int)next_row, bar_z);
+                // every thread has read its z rows: prefetch the next chunk's (UNB: the
+                // two g boxes of the z region now, the two in V^T once the RHS read it)
+                if (has_next) {
+                    if (UNB) {
+                        ptx::mbar_arrive_expect_tx(bar_z, 32768);
+                        for (int b = 0; b < 2; ++b)
+                            ptx::tma_load_2d(sm + g_box_off<false>(b), &tm_z, hx + 32 * b, (int)next_row, bar_z);
+                    } else {
+                        tma_2box(sm + OFF_Z, &tm_z, hx, (int)next_row, bar_z);
+                    }
+                }
+                if (UNB)   // this chunk's diagonal tiles, behind P
+                    bulk_load(sm + OFF_DG, reinterpret_cast<const uint8_t *>(
+                                  p.diag + diag_slot(p.diag_stride, h, bos, seq, cidx) * 2048),
+                              8192, bar_d);
                 // Gram/P: D[r][tile_off(a) + s] = [Q^;K^][r] . B[tile_off(a) + s], all four tiles
                 mma_k<8>(tmem + TM_G, sbase + OFF_QK, 16384u, sbase + OFF_GB, GB_KBLK,
                          ptx::idesc_bf16_f32(128, 160), false);
@@ -866,6 +926,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             ++g_issued; ++s_issued;
             if (has_next) ++z_issued;
+            if (UNB) ++d_issued;
             // while the MMAs run: V^T
             if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
             phase_vt(x, nvalid);
@@ -874,8 +935,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
             if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, hx, (int)next_row, bar_qk);
             if (has_next) ++qk_issued;
+            if (UNB) {
+                if (ptx::mbar_wait(bar_d, d_done & 1, kWaitBudget)) ++d_done; else *s_abort = 1;
+            }
             ptx::tc_fence_after_sync();
-            phase_extract_PL(x, OFF_PB);
+            phase_extract_PL(x, OFF_PB, UNB ? reinterpret_cast<const float *>(sm + OFF_DG) : nullptr);
             __syncthreads();
             phase_diag(x);
             __syncthreads();
@@ -895,6 +959,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mma_k<4>(tmem + TM_D2, sbase + OFF_RU, 0u, sbase + OFF_TB, 0u,
                          ptx::idesc_bf16_f32(128, 64), false);
                 ptx::mma_commit(bar_m);
+                if (UNB && has_next)   // the RHS has read V^T: the next chunk's other two g boxes
+                    for (int b = 2; b < 4; ++b)
+                        ptx::tma_load_2d(sm + g_box_off<false>(b), &tm_z, hx + 32 * b, (int)next_row, bar_z);
             }
             ++m_issued;
             // (loaded into the register untouched: the load latency hides behind phases C-D)
@@ -950,6 +1017,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         while (g_done < g_issued && ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done;
         while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
         while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
+        while (d_done < d_issued && ptx::mbar_wait(bar_d, d_done & 1, kWaitBudget)) ++d_done;
     }
     if (tid == 0) ptx::bulk_wait_all();   // output stores done before shared memory goes away
     ptx::tc_fence_before_sync();
@@ -1012,37 +1080,12 @@ struct SplitParams {
     uint8_t *seg_out;          // [chains][segs] cells of SEG_CELL bytes: S0 (from a zero state, float32
                                // [c][j]) and M (bf16 tile M[c'][c], the scan's B operand layout)
     float *seg_in;             // [chains][segs][128][128]: the state each segment starts from
-    // unbounded log-decay (kda_chunk_prefill_logdecay): inputs of the diagonal
-    // tiles' pre-pass, and its output per record slot ([L | P][tile][16][16])
-    const __nv_bfloat16 *q, *k;
-    const float *g;
-    float *diag;
+    // unbounded log-decay (kda_chunk_prefill_logdecay): the diagonal tiles of
+    // every chunk ([L | P][tile][16][16] float32), at diag_slot()
+    const float *diag;
+    int64_t diag_stride;
 };
 
-
-__device__ __forceinline__ void bulk_store(uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(gdst)),
-                 "r"(ptx::smem_addr(ssrc)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_copy_in(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
-                                             uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            ptx::smem_addr(sdst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar))
-        : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
-                                          uint64_t *bar) {
-    ptx::mbar_arrive_expect_tx(bar, bytes);
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            ptx::smem_addr(sdst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar))
-        : "memory");
-}
 
 struct ItemInfo {
     int chain, h, c;
@@ -1073,43 +1116,73 @@ __device__ __forceinline__ bool item_info(const SplitParams &p, int it, ItemInfo
 // and right factors, so its entries are summed position pair by position pair:
 //   L'_ts = sum_c k_tc k_sc 2^(G_tc - G_sc),  P_ts = sum_c q_tc k_sc 2^(G_tc - G_sc),
 // s <= t in the same tile (L' without beta and only for s < t), with G the
-// tile-local inclusive log2 decay, so every power is <= 1.  One CTA per work
-// item of the window (as in the intra-chunk kernel); rows past the sequence end
-// count as zero keys and queries.
+// tile-local inclusive log2 decay, so every power is <= 1.  Rows past the
+// sequence end count as zero keys and queries.
+//
+// Storage: 2048 floats per (head, chunk), at slot h S + (bos >> 6) + seq + c
+// for chunk c of sequence seq starting at token bos, S = (T >> 6) + N + 1:
+// sequences never share a slot and the slots of a head fit in S.
+struct DiagParams {
+    const __nv_bfloat16 *q, *k;
+    const float *g;
+    const int32_t *cu_seqlens;
+    int64_t total_tokens;
+    int num_seqs;
+    int H;
+    float *diag;
+    int64_t stride;            // S
+};
 constexpr int DG_P = 129;   // padded row of the staged tiles
 constexpr uint32_t SMEM_DIAG = 3 * 64 * DG_P * 4;
 
+// One CTA per slot, persistent over slots; a slot finds its sequence by
+// binary search on the slot bases.
 __global__ void __launch_bounds__(256)
-diag_tiles_kernel(const SplitParams p) {
+diag_tiles_kernel(const DiagParams p) {
     extern __shared__ float dsm[];
     float *Kt = dsm, *Qt = dsm + 64 * DG_P, *Gt = dsm + 2 * 64 * DG_P;
     const int tid = threadIdx.x;
-    const int n_items = p.num_seqs * p.H * p.wn;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int64_t n_slots = (int64_t)p.H * p.stride;
+    for (int64_t it = blockIdx.x; it < n_slots; it += gridDim.x) {
+        const int h = (int)(it / p.stride);
+        const int64_t sl = it - (int64_t)h * p.stride;
+        int lo = 0, hi = p.num_seqs - 1;     // the last sequence whose base is <= sl
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)(p.cu_seqlens[mid] >> 6) + mid <= sl) lo = mid; else hi = mid - 1;
+        }
+        const int seq = lo;
+        int64_t bos = p.cu_seqlens[seq], eos = p.cu_seqlens[seq + 1];
+        if (bos < 0 || eos < bos || eos > p.total_tokens) continue;   // reported by the main kernel
+        const int64_t c = sl - ((bos >> 6) + seq);
+        const int64_t nch = (eos - bos + C - 1) / C;
+        if (c < 0 || c >= nch) continue;   // uniform over the CTA
         ItemInfo cur;
-        if (!item_info(p, it, cur)) continue;   // uniform over the CTA
+        cur.h = h;
+        cur.row0 = bos + c * C;
+        cur.nvalid = (int)((eos - cur.row0) < C ? (eos - cur.row0) : C);
         const int64_t rs = (int64_t)p.H * D;     // row stride of q, k, g
-        __syncthreads();                         // the previous item's tiles are consumed
+        __syncthreads();                         // the previous slot's tiles are consumed
         for (int e = tid; e < 64 * D; e += 256) {
-            const int t = e >> 7, c = e & (D - 1);
+            const int t = e >> 7, cc = e & (D - 1);
             const bool ok = t < cur.nvalid;
-            const int64_t gi = (cur.row0 + t) * rs + (int64_t)cur.h * D + c;
-            Kt[t * DG_P + c] = ok ? __bfloat162float(p.k[gi]) : 0.f;
-            Qt[t * DG_P + c] = ok ? __bfloat162float(p.q[gi]) : 0.f;
-            Gt[t * DG_P + c] = ok ? fmaxf(p.g[gi], -100.f) * kLog2e : 0.f;
+            const int64_t gi = (cur.row0 + t) * rs + (int64_t)cur.h * D + cc;
+            Kt[t * DG_P + cc] = ok ? __bfloat162float(p.k[gi]) : 0.f;
+            Qt[t * DG_P + cc] = ok ? __bfloat162float(p.q[gi]) : 0.f;
+            Gt[t * DG_P + cc] = ok ? fmaxf(p.g[gi], -100.f) * kLog2e : 0.f;
         }
         __syncthreads();
         for (int e = tid; e < 4 * D; e += 256) {   // tile-local inclusive sums, per (tile, channel)
-            const int a = e >> 7, c = e & (D - 1);
+            const int a = e >> 7, cc = e & (D - 1);
             float run = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                run += Gt[(16 * a + i) * DG_P + c];
-                Gt[(16 * a + i) * DG_P + c] = run;
+                run += Gt[(16 * a + i) * DG_P + cc];
+                Gt[(16 * a + i) * DG_P + cc] = run;
             }
         }
         __syncthreads();
-        float *out = p.diag + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * 2048;
+        float *out = p.diag + it * 2048;
         // the 136 pairs s <= t of each tile, numbered r = t (t + 1) / 2 + s, all
         // lanes busy; the diagonal (factor 1) through the same expression
         for (int e = tid; e < 4 * 136; e += 256) {
@@ -1202,7 +1275,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     auto load_gz = [&](int hx, int row) {   // z tile, or the four g boxes
         if (UNB) {
             ptx::mbar_arrive_expect_tx(bar_z, 32768);
-            for (int b = 0; b < 4; ++b) ptx::tma_load_2d(sm + g_box_off(b), &tm_z, hx + 32 * b, row, bar_z);
+            for (int b = 0; b < 4; ++b) ptx::tma_load_2d(sm + g_box_off<true>(b), &tm_z, hx + 32 * b, row, bar_z);
         } else {
             tma_2box(sm + OFF_Z, &tm_z, hx, row, bar_z);
         }
@@ -1266,7 +1339,8 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (has_next) load_gz(nhx, (int)nxt.row0);
             if (UNB)   // this item's diagonal tiles, into the space behind P
                 bulk_load(sm + OFF_DG, reinterpret_cast<const uint8_t *>(
-                                           p.diag + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * 2048),
+                              p.diag + diag_slot(p.diag_stride, cur.h, cur.row0 - (int64_t)cur.c * C,
+                                                 cur.chain / H, cur.c) * 2048),
                           8192, bar_d);
             mma_k<8>(tmem + TM_G, sbase + OFF_QK, 16384u, sbase + OFF_GB, GB_KBLK,
                      ptx::idesc_bf16_f32(128, 160), false);
@@ -2103,11 +2177,40 @@ size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H) {
 // the fused kernel or an intra and a state kernel per window.
 // The chunked path for a given (unbounded) log-decay: the segment-scan plan
 // plus the diagonal tiles of every chunk; 0 when that plan does not apply.
+static int64_t diag_stride(int64_t total, int num_seqs) { return (total >> 6) + num_seqs + 1; }
+
+static cudaError_t launch_diag_tiles(const void *q, const void *k, const float *g, const int32_t *cu,
+                                     int64_t total, int num_seqs, int H, float *diag, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(tc::diag_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc::SMEM_DIAG);
+    if (e != cudaSuccess) return e;
+    tc::DiagParams dp;
+    dp.q = static_cast<const __nv_bfloat16 *>(q);
+    dp.k = static_cast<const __nv_bfloat16 *>(k);
+    dp.g = g;
+    dp.cu_seqlens = cu;
+    dp.total_tokens = total;
+    dp.num_seqs = num_seqs;
+    dp.H = H;
+    dp.diag = diag;
+    dp.stride = diag_stride(total, num_seqs);
+    const int64_t slots = (int64_t)H * dp.stride;
+    const int64_t grid = 4 * (int64_t)sm_count();
+    // a plain launch: it waits for the schedule (status word) like any kernel
+    tc::diag_tiles_kernel<<<(unsigned)(slots < grid ? slots : grid), 256, tc::SMEM_DIAG, st>>>(dp);
+    return cudaGetLastError();
+}
+
+// The chunked paths for a given (unbounded) log-decay: the segment-scan plan
+// when it applies, else the fused kernel; both plus the diagonal tiles of
+// every chunk.
+static size_t diag_bytes(int64_t total, int num_seqs, int H) {
+    return (size_t)H * (size_t)diag_stride(total, num_seqs) * 8192;
+}
 size_t prefill_tc_logdecay_workspace_bytes(int64_t total, int num_seqs, int H) {
     const ScanPlan c = plan_scan(total, num_seqs, H);
-    if (!c.ok) return 0;
-    const size_t diag_off = (c.bytes + 255) & ~size_t(255);
-    return diag_off + (size_t)num_seqs * H * c.max_chunks * 8192;
+    const size_t base = c.ok ? c.bytes : kWsOrder + sizeof(int32_t) * (size_t)num_seqs;
+    return ((base + 255) & ~size_t(255)) + diag_bytes(total, num_seqs, H);
 }
 
 int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes) {
@@ -2180,7 +2283,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
                                        void *workspace, size_t workspace_bytes, cudaStream_t st) {
     const ScanPlan scan = plan_scan(total, num_seqs, H);
     const size_t need = prefill_tc_logdecay_workspace_bytes(total, num_seqs, H);
-    if (!scan.ok || need == 0 || workspace_bytes < need) return cudaErrorNotSupported;
+    if (workspace_bytes < need) return cudaErrorNotSupported;
     CUtensorMap mq, mk, mv, mg, mo;
     if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) ||
         !make_map(&mv, v, total, H) || !make_map_g(&mg, g, total, H) ||
@@ -2194,11 +2297,26 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     const int64_t chains = (int64_t)num_seqs * H;
-    const void *kernels[5] = {(const void *)tc::prefill_intra_kernel<true>, (const void *)tc::prefill_seg_kernel,
-                              (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel,
-                              (const void *)tc::diag_tiles_kernel};
-    const uint32_t smem[5] = {tc::SMEM_ALLOC, tc::SMEM_SEG, tc::SMEM_SCAN, tc::SMEM_STATE, tc::SMEM_DIAG};
-    for (int i = 0; i < 5; ++i)
+    if (!scan.ok) {   // the fused kernel in its unbounded mode
+        float *diag = reinterpret_cast<float *>(
+            ws + ((kWsOrder + sizeof(int32_t) * (size_t)num_seqs + 255) & ~size_t(255)));
+        if ((e = launch_diag_tiles(q, k, g, cu, total, num_seqs, H, diag, st)) != cudaSuccess) return e;
+        if ((e = cudaFuncSetAttribute(tc::prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)tc::SMEM_ALLOC)) != cudaSuccess)
+            return e;
+        tc::Params prm;
+        prm.A = nullptr; prm.beta = beta; prm.cu_seqlens = cu; prm.initial_state = s0;
+        prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
+        prm.counter = counter; prm.status = status; prm.total_tokens = total;
+        prm.num_seqs = num_seqs; prm.H = H; prm.diag = diag; prm.diag_stride = diag_stride(total, num_seqs);
+        const int grid = (int)(chains < sms ? chains : sms);
+        return launch_pdl(tc::prefill_tc_kernel<true>, (unsigned)grid, tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv,
+                          mg, mo, prm);
+    }
+    const void *kernels[4] = {(const void *)tc::prefill_intra_kernel<true>, (const void *)tc::prefill_seg_kernel,
+                              (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel};
+    const uint32_t smem[4] = {tc::SMEM_ALLOC, tc::SMEM_SEG, tc::SMEM_SCAN, tc::SMEM_STATE};
+    for (int i = 0; i < 4; ++i)
         if ((e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem[i])) != cudaSuccess)
             return e;
@@ -2215,14 +2333,11 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
     sp.seg_len = scan.seg_len;
     sp.seg_out = ws + scan.seg_out_off;
     sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
-    sp.q = static_cast<const __nv_bfloat16 *>(q);
-    sp.k = static_cast<const __nv_bfloat16 *>(k);
-    sp.g = g;
     sp.diag = reinterpret_cast<float *>(ws + ((scan.bytes + 255) & ~size_t(255)));
+    sp.diag_stride = diag_stride(total, num_seqs);
     const int64_t items = chains * scan.max_chunks;
-    // a plain launch: it waits for the schedule (status word) like any kernel
-    tc::diag_tiles_kernel<<<(unsigned)(items < 4 * sms ? items : 4 * sms), 256, tc::SMEM_DIAG, st>>>(sp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_diag_tiles(q, k, g, cu, total, num_seqs, H, const_cast<float *>(sp.diag), st)) != cudaSuccess)
+        return e;
     if ((e = launch_pdl(tc::prefill_intra_kernel<true>, (unsigned)(items < sms ? items : sms),
                         tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mg, sp)) != cudaSuccess)
         return e;
@@ -2279,7 +2394,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.seg_len = scan.seg_len;
         sp.seg_out = ws + scan.seg_out_off;
         sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
-        sp.q = nullptr; sp.k = nullptr; sp.g = nullptr; sp.diag = nullptr;
+        sp.diag = nullptr; sp.diag_stride = 0;
         const int64_t items = chains * scan.max_chunks;
         if ((e = launch_pdl(tc::prefill_intra_kernel<false>, (unsigned)(items < sms ? items : sms),
                             tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
@@ -2316,7 +2431,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.status = status; sp.total_tokens = total; sp.num_seqs = num_seqs; sp.H = H;
         sp.W = plan.W;
         sp.segs = 1; sp.seg_len = 0; sp.seg_out = nullptr; sp.seg_in = nullptr;
-        sp.q = nullptr; sp.k = nullptr; sp.g = nullptr; sp.diag = nullptr;
+        sp.diag = nullptr; sp.diag_stride = 0;
         // fork: the side stream starts after everything already on `st`
         if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
@@ -2342,7 +2457,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         return cudaGetLastError();
     }
 
-    e = cudaFuncSetAttribute(tc::prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc::prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tc::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const int grid = (int)(chains < sms ? chains : sms);
@@ -2350,8 +2465,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     prm.A = A; prm.beta = beta; prm.cu_seqlens = cu; prm.initial_state = s0;
     prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
     prm.counter = counter; prm.status = status; prm.total_tokens = total;
-    prm.num_seqs = num_seqs; prm.H = H;
-    return launch_pdl(tc::prefill_tc_kernel, (unsigned)grid, tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, mo, prm);
+    prm.num_seqs = num_seqs; prm.H = H; prm.diag = nullptr; prm.diag_stride = 0;
+    return launch_pdl(tc::prefill_tc_kernel<false>, (unsigned)grid, tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz,
+                      mo, prm);
 }
 
 }  // namespace kda

@@ -135,13 +135,13 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
  * bound, the reciprocal cumulative decay of a chunk could overflow, and the
  * diagonal 16-token tiles needed a special position-pair path instead of the
  * dense tensor-core one.  That is what this call does for bf16 with dk = dv =
- * 128 on batches of few long sequences, when the workspace holds
- * kda_prefill_logdecay_workspace_size() bytes: the diagonal tiles are summed
- * pair by pair in a pre-pass and every other factor is formed with a
- * non-positive exponent, then the segment-scan plan runs as for
- * kda_chunk_prefill.  Otherwise it runs the token-serial kernel (any dtype and
- * head size; a 4-byte workspace suffices).  Both are exact for any decay; the
- * measure of what the bound buys.
+ * 128 when the workspace holds kda_prefill_logdecay_workspace_size() bytes:
+ * the diagonal tiles of every chunk are summed pair by pair in a pre-pass and
+ * every other factor is formed with a non-positive exponent, in the
+ * segment-scan plan for batches of few long sequences and in the fused kernel
+ * otherwise.  With a smaller workspace, or another dtype or head size, it runs
+ * the token-serial kernel (a 4-byte workspace suffices).  Both are exact for
+ * any decay; the measure of what the bound buys.
  *   g          [total_tokens, H, dk] float32 (replaces z and A), 16-byte aligned
  *   workspace  16-byte aligned; at least 4 bytes (the status word)
  * All other arguments as for kda_chunk_prefill.

@@ -124,3 +124,23 @@ def test_chunked_unbounded_path_on_bounded_gate():
     torch.cuda.synchronize()
     assert_close("outputs", out, ref_out.double().cpu().numpy(), torch.bfloat16)
     assert_close("states", fin, ref_fin.double().cpu().numpy(), torch.bfloat16)
+
+
+def test_chunked_unbounded_many_chains_against_oracle():
+    """Many (sequence, head) chains: the fused kernel in its unbounded mode
+    (diagonal tiles from the pre-pass, g in four float32 boxes), against the
+    oracle, with a nonzero initial state and ragged lengths."""
+    dev = need_gpu()
+    rng = np.random.default_rng(67)
+    lens = [int(x) for x in rng.integers(1, 300, size=30)]
+    w = inputs.custom(lens, H=2, dk=128, dv=128, dtype=torch.bfloat16, init="randn0.1", wid=67)
+    d = inputs.prefill_inputs(w)
+    g = torch.from_numpy(_unbounded_g(w.total_tokens, w.H, 128, 67))
+    x = to_device(d, dev)
+    out, fin = chunk_prefill_logdecay(x["q"], x["k"], x["v"], g.to(dev), x["beta"], x["cu_seqlens"],
+                                      x["initial_state"])
+    torch.cuda.synchronize()
+    ro, rf = oracle.prefill(d["q"], d["k"], d["v"], None, None, d["beta"], d["cu_seqlens"],
+                            d["initial_state"], g=g.numpy())
+    assert_close("outputs", out, ro, torch.bfloat16)
+    assert_close("states", fin, rf, torch.bfloat16)
