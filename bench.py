@@ -374,6 +374,9 @@ def run_gpu(args):
             extra[inputs.workload(wid).name] = _time_large_prefill(kda, inputs, wid, dev, seed,
                                                                    flush, barrier, agg_max, peak,
                                                                    peak_kind)
+        # the varlen batch through the unbounded-decay path (fused kernel, unbounded mode)
+        ablation["varlen"] = _time_large_prefill(kda, inputs, 2, dev, seed, flush, barrier, agg_max,
+                                                 peak, peak_kind, unbounded=True)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
