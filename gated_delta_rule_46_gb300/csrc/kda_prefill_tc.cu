@@ -1135,23 +1135,29 @@ struct DiagParams {
 constexpr int DG_P = 129;   // padded row of the staged tiles
 constexpr uint32_t SMEM_DIAG = 3 * 64 * DG_P * 4;
 
-// One CTA per slot, persistent over slots; a slot finds its sequence by
-// binary search on the slot bases.
+// One CTA per slot, persistent over slots; a slot's sequence is the last one
+// whose base (bos >> 6) + seq is <= the slot (bases increase), found by all
+// threads at once: one load each and a maximum, not a chain of dependent loads.
 __global__ void __launch_bounds__(256)
 diag_tiles_kernel(const DiagParams p) {
     extern __shared__ float dsm[];
+    __shared__ int s_seq;
     float *Kt = dsm, *Qt = dsm + 64 * DG_P, *Gt = dsm + 2 * 64 * DG_P;
     const int tid = threadIdx.x;
     const int64_t n_slots = (int64_t)p.H * p.stride;
     for (int64_t it = blockIdx.x; it < n_slots; it += gridDim.x) {
         const int h = (int)(it / p.stride);
         const int64_t sl = it - (int64_t)h * p.stride;
-        int lo = 0, hi = p.num_seqs - 1;     // the last sequence whose base is <= sl
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)(p.cu_seqlens[mid] >> 6) + mid <= sl) lo = mid; else hi = mid - 1;
-        }
-        const int seq = lo;
+        __syncthreads();                         // the previous slot's tiles and s_seq are consumed
+        if (tid == 0) s_seq = 0;
+        __syncthreads();
+        int best = 0;
+        for (int i = tid; i < p.num_seqs; i += 256)
+            if ((int64_t)(p.cu_seqlens[i] >> 6) + i <= sl) best = i;
+        best = __reduce_max_sync(0xffffffffu, best);
+        if ((tid & 31) == 0 && best > 0) atomicMax(&s_seq, best);
+        __syncthreads();
+        const int seq = s_seq;
         int64_t bos = p.cu_seqlens[seq], eos = p.cu_seqlens[seq + 1];
         if (bos < 0 || eos < bos || eos > p.total_tokens) continue;   // reported by the main kernel
         const int64_t c = sl - ((bos >> 6) + seq);
@@ -1162,7 +1168,6 @@ diag_tiles_kernel(const DiagParams p) {
         cur.row0 = bos + c * C;
         cur.nvalid = (int)((eos - cur.row0) < C ? (eos - cur.row0) : C);
         const int64_t rs = (int64_t)p.H * D;     // row stride of q, k, g
-        __syncthreads();                         // the previous slot's tiles are consumed
         for (int e = tid; e < 64 * D; e += 256) {
             const int t = e >> 7, cc = e & (D - 1);
             const bool ok = t < cur.nvalid;
@@ -1194,13 +1199,19 @@ diag_tiles_kernel(const DiagParams p) {
             const float *kt = Kt + (16 * a + t) * DG_P, *qt = Qt + (16 * a + t) * DG_P;
             const float *ks = Kt + (16 * a + s_) * DG_P;
             const float *gt = Gt + (16 * a + t) * DG_P, *gs = Gt + (16 * a + s_) * DG_P;
-            float l = 0.f, pp = 0.f;
-#pragma unroll 4
-            for (int c = 0; c < D; ++c) {
-                const float f = ks[c] * ex2(gt[c] - gs[c]);
-                l += kt[c] * f;
-                pp += qt[c] * f;
+            // four channels per step into independent partial sums (no long
+            // dependence chain through one accumulator)
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll 2
+            for (int c = 0; c < D; c += 4) {
+                const float f0 = ks[c] * ex2(gt[c] - gs[c]);
+                const float f1 = ks[c + 1] * ex2(gt[c + 1] - gs[c + 1]);
+                const float f2 = ks[c + 2] * ex2(gt[c + 2] - gs[c + 2]);
+                const float f3 = ks[c + 3] * ex2(gt[c + 3] - gs[c + 3]);
+                l0 += kt[c] * f0; l1 += kt[c + 1] * f1; l2 += kt[c + 2] * f2; l3 += kt[c + 3] * f3;
+                p0 += qt[c] * f0; p1 += qt[c + 1] * f1; p2 += qt[c + 2] * f2; p3 += qt[c + 3] * f3;
             }
+            const float l = (l0 + l1) + (l2 + l3), pp = (p0 + p1) + (p2 + p3);
             out[a * 256 + t * 16 + s_] = s_ < t ? l : 0.f;
             out[1024 + a * 256 + t * 16 + s_] = pp;
         }
