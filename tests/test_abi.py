@@ -78,3 +78,34 @@ def test_host_side_validation(lib):
                                     None) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_state_slots_copy(fake, 4, fake, fake, 2, 2, 96, 128, 0, None,
                                     None) == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_logdecay_workspace_sizes(lib):
+    """Host-side plan sizes of the unbounded-decay path: the bounded plan's
+    workspace plus 8 KB of diagonal tiles per (head, chunk slot), slots
+    S = T/64 + N + 1 per head; the minimum for shapes the chunked path skips."""
+    from gated_delta_rule_46_gb300 import kda
+    bf, f32 = kda.KDA_BF16, kda.KDA_F32
+    for T, N, H in ((4096, 1, 16), (611958, 64, 32), (538, 4, 3)):
+        unb = lib.kda_prefill_logdecay_workspace_size(T, N, H, 128, 128, bf)
+        bounded = lib.kda_prefill_workspace_size(T, N, H, 128, 128, bf)
+        diag = H * ((T >> 6) + N + 1) * 8192
+        assert unb >= diag and unb % 256 == 0
+        assert unb >= diag + min(bounded, 256)
+    # float32 or other head sizes: the token-serial kernel, the bounded minimum
+    assert lib.kda_prefill_logdecay_workspace_size(4096, 1, 16, 128, 128, f32) == \
+        lib.kda_prefill_workspace_size(4096, 1, 16, 128, 128, f32)
+    assert lib.kda_prefill_logdecay_workspace_size(4096, 1, 16, 64, 64, bf) == \
+        lib.kda_prefill_workspace_size(4096, 1, 16, 64, 64, bf)
+
+
+def test_bindings_reject_host_tensors():
+    """The product path has no CPU fallback: host tensors are refused before
+    any library call."""
+    import torch
+    from gated_delta_rule_46_gb300 import chunk_prefill_logdecay, state_slots_copy
+    q = torch.zeros(8, 1, 32, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        chunk_prefill_logdecay(q, q, q, q, torch.zeros(8, 1), torch.tensor([0, 8], dtype=torch.int32))
+    with pytest.raises(ValueError):
+        state_slots_copy(torch.zeros(2, 1, 32, 32), torch.zeros(1, dtype=torch.int32), torch.zeros(1, 1, 32, 32))
