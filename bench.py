@@ -285,38 +285,96 @@ def run_gpu(args):
     t_dec = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
     t_total = e_start.elapsed_time(e_end)
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers.  Every step copies its
+    # inputs in from pinned host memory and its outputs back out.  The copies run
+    # on two copy streams, double-buffered against the compute stream: step i's
+    # inputs travel while step i - 1 computes and step i - 1's outputs travel
+    # back.  e2e = work / wall time of the whole pipelined run (first copy in to
+    # last copy out), so a copy that does not overlap counts in full.
     pin = {n: t.pin_memory() for n, t in d1.items() if isinstance(t, torch.Tensor)}
-    host_out1 = torch.empty((T1, H1, 128), dtype=torch.bfloat16).pin_memory()
-    host_fin1 = torch.empty((1, H1, 128, 128), dtype=torch.float32).pin_memory()
+    host_out1 = [torch.empty((T1, H1, 128), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    host_fin1 = [torch.empty((1, H1, 128, 128), dtype=torch.float32).pin_memory() for _ in range(2)]
     pin_steps = [{n: t.pin_memory() for n, t in hs.items()} for hs in host_steps]
-    host_out4 = torch.empty((w4.decode_N, w4.H, 128), dtype=torch.bfloat16).pin_memory()
+    host_out4 = [torch.empty((w4.decode_N, w4.H, 128), dtype=torch.bfloat16).pin_memory()
+                 for _ in range(NS)]
     h2d_pref = sum(t.numel() * t.element_size() for t in pin.values())
-    d2h_pref = host_out1.numel() * 2 + host_fin1.numel() * 4
+    d2h_pref = host_out1[0].numel() * 2 + host_fin1[0].numel() * 4
     h2d_dec = NS * sum(t.numel() * t.element_size() for t in pin_steps[0].values())
-    d2h_dec = NS * host_out4.numel() * 2
-    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    barrier()
-    for i in range(K):
-        flush.fill_(float(i))
-        ee[i][0].record(stream)
+    d2h_dec = NS * host_out4[0].numel() * 2
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    gb = [{n: torch.empty_like(t) for n, t in g1.items() if isinstance(t, torch.Tensor)} for _ in range(2)]
+    ob = [torch.empty_like(out1) for _ in range(2)]
+    fb = [torch.empty_like(fin1) for _ in range(2)]
+    db = [{n: torch.empty_like(t) for n, t in dsteps[0].items()} for _ in range(2)]
+    dob = [torch.empty_like(out4) for _ in range(2)]
+
+    def ev():
+        return torch.cuda.Event()
+
+    def pipelined(n_items, copy_in, compute, copy_out):
+        """n_items steps through the three streams, buffers b = i % 2; returns
+        the wall time in seconds (events on the compute stream)."""
+        in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        used = [False, False]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        for i in range(n_items):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if used[b]:
+                    s_in.wait_event(comp_done[b])     # compute i - 2 has read buffer b
+                copy_in(i, b)
+                in_done[b].record(s_in)
+            stream.wait_event(in_done[b])
+            if used[b]:
+                stream.wait_event(out_done[b])        # outputs of i - 2 have left buffer b
+            compute(i, b)
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                copy_out(i, b)
+                out_done[b].record(s_out)
+            used[b] = True
+        stream.wait_event(out_done[0])
+        stream.wait_event(out_done[1])
+        e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) / 1000.0
+
+    def pref_in(i, b):
         for n, t in pin.items():
-            g1[n].copy_(t, non_blocking=True)
-        prefill()
-        host_out1.copy_(out1, non_blocking=True)
-        host_fin1.copy_(fin1, non_blocking=True)
-        ee[i][1].record(stream)
-        ee[i][2].record(stream)
-        for s in range(NS):
-            x = dsteps[s]
-            for n, t in pin_steps[s].items():
-                x[n].copy_(t, non_blocking=True)
-            kda.decode_step(x["q"], x["k"], x["v"], x["z"], A4, x["beta"], state, out=out4)
-            host_out4.copy_(out4, non_blocking=True)
-        ee[i][3].record(stream)
-    barrier()
-    e2e_pref = [ee[i][0].elapsed_time(ee[i][1]) for i in range(K)]
-    e2e_dec = [ee[i][2].elapsed_time(ee[i][3]) for i in range(K)]
+            gb[b][n].copy_(t, non_blocking=True)
+
+    def pref_compute(i, b):
+        flush.fill_(float(i))
+        x = gb[b]
+        kda.chunk_prefill(x["q"], x["k"], x["v"], x["z"], x["A"], x["beta"], x["cu_seqlens"],
+                          x["initial_state"], final_state=fb[b], out=ob[b], workspace=ws1)
+
+    def pref_out(i, b):
+        host_out1[b].copy_(ob[b], non_blocking=True)
+        host_fin1[b].copy_(fb[b], non_blocking=True)
+
+    def dec_in(i, b):
+        for n, t in pin_steps[i % NS].items():
+            db[b][n].copy_(t, non_blocking=True)
+
+    def dec_compute(i, b):
+        x = db[b]
+        kda.decode_step(x["q"], x["k"], x["v"], x["z"], A4, x["beta"], state, out=dob[b])
+
+    def dec_out(i, b):
+        host_out4[i % NS].copy_(dob[b], non_blocking=True)
+
+    pipelined(2, pref_in, pref_compute, pref_out)            # warm-up of the streams
+    e2e_pref_s = pipelined(K, pref_in, pref_compute, pref_out)
+    e2e_dec_s = pipelined(K * NS, dec_in, dec_compute, dec_out)
+    # the copies alone (no compute), for the achieved host<->device rate
+    t_copy = pipelined(K, pref_in, lambda i, b: None, pref_out)
+    copy_gbs = K * (h2d_pref + d2h_pref) / t_copy / 1e9
 
     def agg_max(x):
         return max_over_ranks(x, world, dev)
@@ -324,8 +382,8 @@ def run_gpu(args):
     tp = agg_max(sum(t_pref) / 1000.0)
     td = agg_max(sum(t_dec) / 1000.0)
     tt = agg_max(t_total / 1000.0)
-    e2p = agg_max(sum(e2e_pref) / 1000.0)
-    e2d = agg_max(sum(e2e_dec) / 1000.0)
+    e2p = agg_max(e2e_pref_s)
+    e2d = agg_max(e2e_dec_s)
     ok_status = kda.check_device_status(ws1)
 
     pref_tokens = world * K * T1
@@ -342,19 +400,25 @@ def run_gpu(args):
     per_launch_dec = (sum(t_dec) / (K * NS)) / 1000.0
     ach_pref = alg_pref / per_launch_pref / 1e9
     ach_dec = alg_dec / per_launch_dec / 1e9
+    traffic_dec = _ncu_traffic("decode_kernel", "kda_simt.cu")
     roof_dec = {"kernel": "decode_kernel<bf16,128,128>", "bound": "hbm", "achieved": ach_dec,
                 "peak": peak, "unit": "GB/s", "frac": ach_dec / peak,
-                "traffic": _ncu_traffic("decode_kernel", "kda_simt.cu"),
+                "traffic": traffic_dec,
                 "algorithmic_bytes_per_launch": alg_dec, "peak_source": peak_kind,
                 "us_per_launch": per_launch_dec * 1e6}
+    if traffic_dec:   # the same launch time over the DRAM bytes ncu counted
+        roof_dec["frac_dram"] = traffic_dec / per_launch_dec / 1e9 / peak
     plan = {2: "schedule + fused prefill_tc_kernel",
             5: "schedule, intra-chunk, segment maps, scan, segment state pass"}.get(
                 L_pref, "schedule, then an intra-chunk and a state-pass kernel per window")
+    traffic_pref = _ncu_traffic("kda_chunk_prefill_T4096_H16", "kda_prefill_tc.cu")
     roof_pref = {"kernel": f"kda_chunk_prefill ({L_pref} launches: {plan})", "bound": "hbm",
                  "achieved": ach_pref, "peak": peak, "unit": "GB/s", "frac": ach_pref / peak,
-                 "traffic": _ncu_traffic("kda_chunk_prefill_T4096_H16", "kda_prefill_tc.cu"),
+                 "traffic": traffic_pref,
                  "algorithmic_bytes_per_launch": alg_pref, "peak_source": peak_kind,
                  "us_per_launch": per_launch_pref * 1e6}
+    if traffic_pref:
+        roof_pref["frac_dram"] = traffic_pref / per_launch_pref / 1e9 / peak
 
     # ---- the decode workload through kda_decode_tokens: 8 tokens per call from a
     # slot pool (the 256 states scattered over 512 slots), 16 calls = 128 tokens
@@ -397,12 +461,16 @@ def run_gpu(args):
                        "l2": "flushed before every prefill (256 MB write); decode state 537 MB > L2"},
             "decode": {"value": dec_value, "unit": "tokens/s", "us_per_step": per_launch_dec * 1e6,
                        "roofline": roof_dec},
-            "roofline": roof_dec,
-            "roofline_prefill": roof_pref,
+            # `value` is the prefill's tokens/s, so `roofline` is the prefill call's;
+            # the decode kernel (most of the step's time) is beside it
+            "roofline": roof_pref,
+            "roofline_decode": roof_dec,
             "prefill_us_per_call": per_launch_pref * 1e6,
             "e2e": {"value": pref_tokens / e2p, "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d_pref + h2d_dec, "d2h_bytes_per_step": d2h_pref + d2h_dec,
-                    "decode_value": dec_tokens / e2d},
+                    "decode_value": dec_tokens / e2d,
+                    "copies": "two copy streams, double-buffered against compute",
+                    "copy_gbs_alone": copy_gbs},
             "decode_tokens": multi,
             "prefill_large": extra,
             "prefill_unbounded_gate": ablation,

@@ -6,6 +6,7 @@
 
 #include "kda.h"
 #include "kda_common.cuh"
+#include "kda_testing.h"
 
 namespace kda {
 cudaError_t launch_gate(const void *z, bool bf16, const float *A, float *g, int64_t n_tokens,
@@ -29,6 +30,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
                                        int64_t total, int H, const float *s0, float *s1, void *out,
                                        void *workspace, size_t workspace_bytes, cudaStream_t st);
 int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes);
+void set_test_expire(int mask);
 cudaError_t launch_state_slots(float *pool, int pool_size, const int32_t *slots, float *states,
                                int N, int H, int dk, int dv, bool to_pool, uint32_t *status,
                                cudaStream_t st);
@@ -229,6 +231,8 @@ kda_status_t kda_state_slots_copy(float *state_pool, int pool_size, const int32_
                                              to_pool != 0, status,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
+
+void kda_testing_expire_next_wait(int kernels) { kda::set_test_expire(kernels); }
 
 kda_status_t kda_check_device_status(const void *workspace, kda_stream_t stream) {
     if (!workspace) return KDA_ERR_INVALID_ARG;

@@ -41,15 +41,22 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
-cudaError_t scratch_on_current_device(void **out) {
+// Device address of the scratch on the current device.  Outside a stream
+// capture it is looked up on every call (with the device current): after a
+// host-side device reset the library's module is loaded anew and the array
+// may move, so a cached address could be stale.  During a capture (when a
+// lookup that loads the module must not happen) the address cached by the
+// last call outside a capture is used.
+cudaError_t scratch_on_current_device(cudaStream_t st, void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(st, &cap);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
@@ -81,9 +88,9 @@ extern "C" kda_status_t kda_chunk_prefill_noalloc(
     if (!cu_seqlens || !A) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !z || !beta || !out)) return KDA_ERR_INVALID_ARG;
 
-    void *scratch = nullptr;
-    if (scratch_on_current_device(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *scratch = nullptr;
+    if (scratch_on_current_device(st, &scratch) != cudaSuccess) return KDA_ERR_CUDA;
     const bool tc = dtype == KDA_BF16 && dk == 128 && dv == 128 && total_tokens > 0 &&
                     aligned16(q) && aligned16(k) && aligned16(v) && aligned16(z) &&
                     aligned16(out);

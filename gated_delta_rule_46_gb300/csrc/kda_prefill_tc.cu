@@ -46,9 +46,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kda_common.cuh"
+#include "kda_testing.h"
 #include "sm100_ptx.cuh"
 
 namespace kda {
@@ -105,6 +107,21 @@ constexpr uint32_t TM_D2 = 320;        // U^T 128 x 64
 constexpr uint32_t TM_D3 = 384;        // dS^T 128 x 128
 
 constexpr long long kWaitBudget = 2000000000LL;   // cycles (about one second)
+
+// Test support (kda_testing_expire_next_wait): CTA 0 of the kernels named by a
+// bit of `test_expire` makes one bounded wait on an mbarrier that nothing ever
+// arrives at, with this short budget, before its first chunk.  The wait runs
+// out like one whose copy never landed, and the kernel takes its ordinary
+// timeout path: record KDA_ERR_DEVICE_TIMEOUT, let the copies and MMAs in
+// flight land, free TMEM, return.
+constexpr long long kTestWaitBudget = 1LL << 21;   // cycles (about a millisecond)
+enum : int {
+    kExpireFused = KDA_TESTING_FUSED, kExpireIntra = KDA_TESTING_INTRA, kExpireSeg = KDA_TESTING_SEGMENT,
+    kExpireScan = KDA_TESTING_SCAN, kExpireState = KDA_TESTING_STATE
+};
+__device__ __forceinline__ bool test_wait_expires(int mask, int bit, uint64_t *bar_never) {
+    return (mask & bit) && blockIdx.x == 0 && !ptx::mbar_wait(bar_never, 0, kTestWaitBudget);
+}
 
 // first row (and TMEM column) of right-factor tile a: 0, 16, 48, 96
 __device__ __forceinline__ int tile_off(int a) { return 8 * a * (a + 1); }
@@ -778,6 +795,7 @@ struct Params {
     int H;
     const float *diag;         // unbounded mode: diagonal tiles per chunk (diag_slot)
     int64_t diag_stride;
+    int test_expire;           // kExpire* bits (test support), 0 otherwise
 };
 
 __device__ __forceinline__ void tma_qk(uint8_t *sm, const CUtensorMap *tq, const CUtensorMap *tk,
@@ -816,6 +834,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t *bar_s = bar_qk + 4;      // state MMA done
     uint64_t *bar_m = bar_qk + 5;      // U MMA, then output/state MMAs done
     uint64_t *bar_d = bar_qk + 6;      // UNB: the chunk's diagonal tiles staged (behind P)
+    uint64_t *bar_never = bar_qk + 7;  // test support: nothing arrives here
     constexpr uint32_t OFF_DG = OFF_OST + 8192;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + OFF_SLOT);
     volatile int *s_work = reinterpret_cast<volatile int *>(sm + OFF_SLOT + 4);
@@ -825,7 +844,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int64_t rowstride = (int64_t)H * D;
 
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) ptx::mbar_init(bar_qk + i, 1);
+        for (int i = 0; i < 8; ++i) ptx::mbar_init(bar_qk + i, 1);
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
@@ -892,6 +911,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
             // =============================== phase A: gate, cumulative decay, operands
             if (tid < C) x.s_beta[tid] = beta_next;
+            if (cidx == 0 && test_wait_expires(p.test_expire, kExpireFused, bar_never)) *s_abort = 1;
             phase_gate_operands<false, UNB>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
@@ -1084,6 +1104,7 @@ struct SplitParams {
     // every chunk ([L | P][tile][16][16] float32), at diag_slot()
     const float *diag;
     int64_t diag_stride;
+    int test_expire;           // kExpire* bits (test support), 0 otherwise
 };
 
 
@@ -1259,6 +1280,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint64_t *bar_v = bar_qk + 2;
     uint64_t *bar_g = bar_qk + 3;      // Gram/P MMA, then W/U~ MMAs done
     uint64_t *bar_d = bar_qk + 4;      // UNB: the item's diagonal tiles staged
+    uint64_t *bar_never = bar_qk + 7;  // test support: nothing arrives here
     // UNB: the diagonal tiles are staged behind P (free until U~^T is staged)
     constexpr uint32_t OFF_DG = OFF_PB + 8192;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + OFF_SLOT);
@@ -1267,7 +1289,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int H = p.H;
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) ptx::mbar_init(bar_qk + i, 1);
+        for (int i = 0; i < 8; ++i) ptx::mbar_init(bar_qk + i, 1);
         ptx::fence_mbar_init();
         *s_abort = 0;
     }
@@ -1319,6 +1341,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int64_t b = p.cu_seqlens[tid], e = p.cu_seqlens[tid + 1];
         if (b < 0 || e < b || e > p.total_tokens) report_status(p.status, kDevBadSeqlens);
     }
+    bool first_item = true;
     while (it < n_items) {
         int nit = it + gridDim.x;
         while (nit < n_items && !item_info(p, nit, nxt)) nit += gridDim.x;
@@ -1339,6 +1362,8 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (tid < nxt.nvalid) beta_cur = p.beta[(nxt.row0 + tid) * H + nxt.h];
         }
 
+        if (first_item && test_wait_expires(p.test_expire, kExpireIntra, bar_never)) *s_abort = 1;
+        first_item = false;
         phase_gate_operands<true, UNB>(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
         if (tid == 0) ptx::bulk_wait_read();   // -W and U~^T staging free for this item
         ptx::fence_async_smem();
@@ -1515,8 +1540,9 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     const bool last = w0 + wn >= nchunks;
     if (w0 >= c_end && !(first && nchunks == 0)) return;   // nothing to do here (uniform per CTA)
 
+    uint64_t *bar_never = bar_st + 7;   // test support: nothing arrives here
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) ptx::mbar_init(bar_st + i, 1);
+        for (int i = 0; i < 8; ++i) ptx::mbar_init(bar_st + i, 1);
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tm_o);
         *s_abort = 0;
@@ -1550,6 +1576,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         if (ptx::mbar_wait(bar_st, st_done[0] & 1, kWaitBudget)) ++st_done[0]; else *s_abort = 1;
         preload_u(x, TS_D1, sm + REC_UT);
     }
+    if (test_wait_expires(p.test_expire, kExpireState, bar_never)) *s_abort = 1;
     ptx::fence_async_smem();
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -1736,8 +1763,9 @@ prefill_seg_kernel(const SplitParams p) {
     const int c_end = (c0 + p.seg_len < nchunks) ? c0 + p.seg_len : nchunks;
     if (c0 >= c_end || c_end >= nchunks) return;   // empty, or the last segment (nobody needs its map)
 
+    uint64_t *bar_never = bar_st + 7;   // test support: nothing arrives here
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) ptx::mbar_init(bar_st + i, 1);
+        for (int i = 0; i < 8; ++i) ptx::mbar_init(bar_st + i, 1);
         ptx::fence_mbar_init();
         *s_abort = 0;
     }
@@ -1766,6 +1794,7 @@ prefill_seg_kernel(const SplitParams p) {
     load_identity(x, TG_M, SG_MT);          // M = I
     if (ptx::mbar_wait(bar_st, st_done[0] & 1, kWaitBudget)) ++st_done[0]; else *s_abort = 1;
     preload_u64(x, TG_U, sm + SG_UT);
+    if (test_wait_expires(p.test_expire, kExpireSeg, bar_never)) *s_abort = 1;
     ptx::fence_async_smem();
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -1896,8 +1925,9 @@ prefill_scan_kernel(const __grid_constant__ CUtensorMap tm_s0, const __grid_cons
     const int nseg = (nchunks + p.seg_len - 1) / p.seg_len;
     if (nseg <= 1) return;   // only the first segment runs, from the initial state
 
+    uint64_t *bar_never = bar + 5;                               // test support: nothing arrives here
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) ptx::mbar_init(bar + i, 1);
+        for (int i = 0; i < 6; ++i) ptx::mbar_init(bar + i, 1);
         ptx::fence_mbar_init();
         *s_abort = 0;
         ptx::prefetch_tensormap(&tm_s0);
@@ -1971,6 +2001,7 @@ prefill_scan_kernel(const __grid_constant__ CUtensorMap tm_s0, const __grid_cons
     read_row(SC_S0, X);
     ptx::tmem_st32(lane_base, X);   // accumulator 0 = S0_0 block
     ptx::tmem_st_wait();
+    if (test_wait_expires(p.test_expire, kExpireScan, bar_never)) *s_abort = 1;
     // Step g accumulates S_in(g + 1) in TMEM buffer g & 1 (32 columns each);
     // writing S_in(g) out and staging S0_(g+1) into the other buffer overlap it.
     for (int g = 0; g + 1 < nseg; ++g) {
@@ -2264,6 +2295,11 @@ static cudaError_t side_stream(SideStream **out) {
 cudaError_t launch_schedule(const int32_t *cu, int num_seqs, int32_t *order, uint32_t *counter,
                             uint32_t *status, cudaStream_t st);
 
+// Test support: the kExpire* bits the next tensor-core prefill call passes to
+// its kernels (kda_testing_expire_next_wait); taken, and cleared, by that call.
+static std::atomic<int> g_test_expire{0};
+void set_test_expire(int mask) { g_test_expire.store(mask); }
+
 // Launches a kernel with programmatic stream serialization: it may start
 // while the previous kernel of the stream finishes and waits for that
 // kernel's results in ptx::pdl_wait().
@@ -2295,6 +2331,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
     const ScanPlan scan = plan_scan(total, num_seqs, H);
     const size_t need = prefill_tc_logdecay_workspace_bytes(total, num_seqs, H);
     if (workspace_bytes < need) return cudaErrorNotSupported;
+    const int test_expire = g_test_expire.exchange(0);
     CUtensorMap mq, mk, mv, mg, mo;
     if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) ||
         !make_map(&mv, v, total, H) || !make_map_g(&mg, g, total, H) ||
@@ -2320,6 +2357,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
         prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
         prm.counter = counter; prm.status = status; prm.total_tokens = total;
         prm.num_seqs = num_seqs; prm.H = H; prm.diag = diag; prm.diag_stride = diag_stride(total, num_seqs);
+        prm.test_expire = test_expire;
         const int grid = (int)(chains < sms ? chains : sms);
         return launch_pdl(tc::prefill_tc_kernel<true>, (unsigned)grid, tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv,
                           mg, mo, prm);
@@ -2346,6 +2384,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
     sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
     sp.diag = reinterpret_cast<float *>(ws + ((scan.bytes + 255) & ~size_t(255)));
     sp.diag_stride = diag_stride(total, num_seqs);
+    sp.test_expire = test_expire;
     const int64_t items = chains * scan.max_chunks;
     if ((e = launch_diag_tiles(q, k, g, cu, total, num_seqs, H, const_cast<float *>(sp.diag), st)) != cudaSuccess)
         return e;
@@ -2382,6 +2421,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     const int64_t chains = (int64_t)num_seqs * H;
+    const int test_expire = g_test_expire.exchange(0);
 
     const ScanPlan scan = plan_scan(total, num_seqs, H);
     if (scan.ok && workspace_bytes >= scan.bytes) {
@@ -2406,6 +2446,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.seg_out = ws + scan.seg_out_off;
         sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
         sp.diag = nullptr; sp.diag_stride = 0;
+        sp.test_expire = test_expire;
         const int64_t items = chains * scan.max_chunks;
         if ((e = launch_pdl(tc::prefill_intra_kernel<false>, (unsigned)(items < sms ? items : sms),
                             tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
@@ -2443,6 +2484,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.W = plan.W;
         sp.segs = 1; sp.seg_len = 0; sp.seg_out = nullptr; sp.seg_in = nullptr;
         sp.diag = nullptr; sp.diag_stride = 0;
+        sp.test_expire = test_expire;
         // fork: the side stream starts after everything already on `st`
         if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
@@ -2477,6 +2519,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
     prm.counter = counter; prm.status = status; prm.total_tokens = total;
     prm.num_seqs = num_seqs; prm.H = H; prm.diag = nullptr; prm.diag_stride = 0;
+    prm.test_expire = test_expire;
     return launch_pdl(tc::prefill_tc_kernel<false>, (unsigned)grid, tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz,
                       mo, prm);
 }

@@ -18,6 +18,9 @@ from . import build as _build
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_TIMEOUT = range(5)
 KDA_F32, KDA_BF16 = 0, 1
+# kernels of the tensor-core prefill, as named by include/kda_testing.h
+KDA_TESTING_FUSED, KDA_TESTING_INTRA, KDA_TESTING_SEGMENT, KDA_TESTING_SCAN, KDA_TESTING_STATE = (
+    1, 2, 4, 8, 16)
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +70,8 @@ def lib():
             L.kda_prefill_kernel_launches.restype = I
             L.kda_check_device_status.argtypes = [P, P]
             L.kda_check_device_status.restype = I
+            L.kda_testing_expire_next_wait.argtypes = [I]
+            L.kda_testing_expire_next_wait.restype = None
             _lib = L
     return _lib
 
@@ -103,6 +108,12 @@ def _check(t, name, shape=None, dtype=None, device=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def _on(device):
+    """Makes `device` current for a call: the library launches on the current
+    device and takes torch's current stream of that device."""
+    return torch.cuda.device(device)
+
+
 def _raise(status, what):
     if status != KDA_OK:
         raise KDAError(status, what)
@@ -116,8 +127,9 @@ def gate(z: torch.Tensor, A: torch.Tensor, g_out: torch.Tensor | None = None, st
     if g_out is None:
         g_out = torch.empty((T, H, dk), dtype=torch.float32, device=z.device)
     _check(g_out, "g_out", (T, H, dk), torch.float32, z.device)
-    _raise(lib().kda_gate(_ptr(z), _dtype_code(z), _ptr(A), _ptr(g_out), T, H, dk,
-                          _stream(stream)), "kda_gate")
+    with _on(z.device):
+        _raise(lib().kda_gate(_ptr(z), _dtype_code(z), _ptr(A), _ptr(g_out), T, H, dk,
+                              _stream(stream)), "kda_gate")
     return g_out
 
 
@@ -159,10 +171,11 @@ def chunk_prefill(q, k, v, z, A, beta, cu_seqlens, initial_state=None, final_sta
     if workspace is None:
         workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
     _check(workspace, "workspace", None, torch.uint8, dev)
-    st = lib().kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
-                                 _ptr(cu_seqlens), N, T, H, dk, dv, _dtype_code(q),
-                                 _ptr(initial_state), _ptr(final_state), _ptr(out),
-                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    with _on(dev):
+        st = lib().kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                     _ptr(cu_seqlens), N, T, H, dk, dv, _dtype_code(q),
+                                     _ptr(initial_state), _ptr(final_state), _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _stream(stream))
     _raise(st, "kda_chunk_prefill")
     return out, final_state
 
@@ -200,10 +213,12 @@ def chunk_prefill_logdecay(q, k, v, g, beta, cu_seqlens, initial_state=None, fin
     if workspace is None:
         workspace = torch.zeros(logdecay_workspace_size(T, N, H, dk, dv, q.dtype), dtype=torch.uint8,
                                 device=dev)
-    st = lib().kda_chunk_prefill_logdecay(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                                          _ptr(cu_seqlens), N, T, H, dk, dv, _dtype_code(q),
-                                          _ptr(initial_state), _ptr(final_state), _ptr(out),
-                                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(workspace, "workspace", None, torch.uint8, dev)
+    with _on(dev):
+        st = lib().kda_chunk_prefill_logdecay(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                              _ptr(cu_seqlens), N, T, H, dk, dv, _dtype_code(q),
+                                              _ptr(initial_state), _ptr(final_state), _ptr(out),
+                                              _ptr(workspace), workspace.numel(), _stream(stream))
     _raise(st, "kda_chunk_prefill_logdecay")
     return out, final_state
 
@@ -234,9 +249,12 @@ def decode_tokens(q, k, v, z, A, beta, state_pool, slot_ids=None, out=None, stat
     if out is None:
         out = torch.empty((N, n, H, dv), dtype=q.dtype, device=dev)
     _check(out, "out", (N, n, H, dv), q.dtype, dev)
-    st = lib().kda_decode_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
-                                 _ptr(state_pool), state_pool.shape[0], _ptr(slot_ids), _ptr(out),
-                                 N, n, H, dk, dv, _dtype_code(q), _ptr(status), _stream(stream))
+    if status is not None:
+        _check(status, "status", None, None, dev)
+    with _on(dev):
+        st = lib().kda_decode_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                     _ptr(state_pool), state_pool.shape[0], _ptr(slot_ids), _ptr(out),
+                                     N, n, H, dk, dv, _dtype_code(q), _ptr(status), _stream(stream))
     _raise(st, "kda_decode_tokens")
     return out
 
@@ -252,8 +270,11 @@ def state_slots_copy(state_pool, slot_ids, states, to_pool=True, status=None, st
     _check(slot_ids, "slot_ids", None, torch.int32, dev)
     N = slot_ids.shape[0]
     _check(states, "states", (N, H, dk, dv), torch.float32, dev)
-    st = lib().kda_state_slots_copy(_ptr(state_pool), P, _ptr(slot_ids), _ptr(states), N, H, dk, dv,
-                                    1 if to_pool else 0, _ptr(status), _stream(stream))
+    if status is not None:
+        _check(status, "status", None, None, dev)
+    with _on(dev):
+        st = lib().kda_state_slots_copy(_ptr(state_pool), P, _ptr(slot_ids), _ptr(states), N, H, dk,
+                                        dv, 1 if to_pool else 0, _ptr(status), _stream(stream))
     _raise(st, "kda_state_slots_copy")
     return states
 
@@ -267,7 +288,9 @@ def prefill_kernel_launches(total_tokens, num_seqs, H, dk, dv, dtype, workspace_
 
 def check_device_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronises the stream and returns the status word kept in the workspace."""
-    return int(lib().kda_check_device_status(_ptr(workspace), _stream(stream)))
+    _check(workspace, "workspace")
+    with _on(workspace.device):
+        return int(lib().kda_check_device_status(_ptr(workspace), _stream(stream)))
 
 
 def decode_step(q, k, v, z, A, beta, state, out=None, stream=None):
@@ -285,9 +308,10 @@ def decode_step(q, k, v, z, A, beta, state, out=None, stream=None):
     if out is None:
         out = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
     _check(out, "out", (N, H, dv), q.dtype, dev)
-    st = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
-                               _ptr(state), _ptr(out), N, H, dk, dv, _dtype_code(q),
-                               _stream(stream))
+    with _on(dev):
+        st = lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                   _ptr(state), _ptr(out), N, H, dk, dv, _dtype_code(q),
+                                   _stream(stream))
     _raise(st, "kda_decode_step")
     return out
 
@@ -322,8 +346,16 @@ def chunk_prefill_noalloc(q, k, v, z, A, beta, cu_seqlens, initial_state=None, f
     if out is None:
         out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
     _check(out, "out", (T, H, dv), q.dtype, dev)
-    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(cu_seqlens), N, T, H,
-            dk, dv, _dtype_code(q), _ptr(initial_state), _ptr(final_state), _ptr(out),
-            _stream(stream))
+    with _on(dev):   # the scratch address and the stream are the current device's
+        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), _ptr(cu_seqlens), N, T,
+                H, dk, dv, _dtype_code(q), _ptr(initial_state), _ptr(final_state), _ptr(out),
+                _stream(stream))
     _raise(st, "kda_chunk_prefill_noalloc")
     return out, final_state
+
+
+def testing_expire_next_wait(kernels: int) -> None:
+    """Test support (include/kda_testing.h): the next bf16 d=128 prefill call's
+    kernels named by the KDA_TESTING_* mask `kernels` see one bounded wait in
+    their first CTA run out, and take their timeout path."""
+    lib().kda_testing_expire_next_wait(int(kernels))

@@ -184,9 +184,10 @@ int kda_prefill_kernel_launches(int64_t total_tokens, int num_seqs, int H, int d
  * loads the library holds until the process exits.
  *   - num_seqs above KDA_NOALLOC_MAX_SEQS returns KDA_ERR_UNSUPPORTED, before
  *     anything is launched.
- *   - The first call on each device looks up the scratch's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Each call looks up the scratch's device address (cudaGetSymbolAddress,
+ *     with the caller's current device) and caches it per device; a call made
+ *     during a stream capture uses the cached address, so make a first call
+ *     on each device before any stream capture.
  *   - Every call on a device shares the one scratch array.  Each call resets
  *     the parts that must start at zero, but calls that overlap on the GPU
  *     (concurrent streams, or other host threads) race on it: serialise them.
@@ -194,7 +195,17 @@ int kda_prefill_kernel_launches(int64_t total_tokens, int num_seqs, int H, int d
  *     in that shared scratch and are not reported by this call; use
  *     kda_chunk_prefill with a workspace and kda_check_device_status to see
  *     them.
- * Results are identical to kda_chunk_prefill's for the same arguments.
+ *   - The scratch has room only for the one-kernel (fused) plan of the
+ *     tensor-core path, never for the few-chain plans.  The results are
+ *     therefore bit-identical to kda_chunk_prefill's when that call also runs
+ *     the fused plan (always, given the minimum workspace; for batches of
+ *     many chains also with kda_prefill_workspace_size() bytes).  For few
+ *     long sequences kda_chunk_prefill with its full workspace sums in another
+ *     order: the two agree within the parity tolerance, not bit for bit, and
+ *     this call is slower there.
+ *   - The lookup is repeated on every call made outside a capture, since the
+ *     address changes if the host resets the device and the library's module
+ *     is loaded anew.
  */
 #define KDA_NOALLOC_MAX_SEQS 16384
 kda_status_t kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
@@ -274,9 +285,18 @@ kda_status_t kda_state_slots_copy(float *state_pool, int pool_size, const int32_
 
 /*
  * kda_check_device_status -- synchronises `stream`, reads the status word that
- * kda_chunk_prefill keeps in `workspace`, and returns KDA_OK or the recorded
- * device-side error (KDA_ERR_DEVICE_TIMEOUT).  Returns KDA_ERR_CUDA if the
- * synchronisation itself fails.
+ * kda_chunk_prefill (or kda_chunk_prefill_logdecay) keeps in `workspace`, and
+ * returns the first device-side condition the last call recorded:
+ *   KDA_OK                  nothing recorded;
+ *   KDA_ERR_INVALID_ARG     malformed cu_seqlens (an offset below 0, above
+ *                           total_tokens, or below the previous one; that
+ *                           sequence was treated as empty), or, for a status
+ *                           word passed to kda_decode_tokens or
+ *                           kda_state_slots_copy, a slot id >= pool_size;
+ *   KDA_ERR_DEVICE_TIMEOUT  a bounded wait inside a kernel expired (the kernel
+ *                           let its copies in flight land and returned; that
+ *                           call's outputs are incomplete).
+ * Returns KDA_ERR_CUDA if the copy or the synchronisation itself fails.
  */
 kda_status_t kda_check_device_status(const void *workspace, kda_stream_t stream);
 

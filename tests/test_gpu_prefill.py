@@ -39,9 +39,11 @@ def test_workload_full(wid):
     assert_close("final state", fin, rf, w.dtype)
 
 
-def test_varlen_workload_sampled_sequences():
-    """The packed 64-sequence batch in one call; the oracle recomputes a sample
-    of whole sequences (longest, shortest and six more) for every head."""
+def test_varlen_workload_every_sequence():
+    """The packed 64-sequence batch in one call (the fused plan, 2,048 chains);
+    the oracle recomputes every sequence for every head, outputs and final
+    states.  The sequences are compared one by one so that host memory stays
+    at one sequence's inputs."""
     dev = need_gpu()
     w = inputs.workload(2)
     g = device_prefill_inputs(w, dev)
@@ -52,17 +54,18 @@ def test_varlen_workload_sampled_sequences():
     assert check_device_status(ws) == 0
     torch.cuda.synchronize()
     assert torch.equal(out, out2), "two identical calls differ"
+    del g, out2
     lens = np.array(w.seq_lens)
-    rng = np.random.default_rng(2024)
-    pick = sorted({int(np.argmax(lens)), int(np.argmin(lens))} |
-                  set(int(i) for i in rng.choice(len(lens), 6, replace=False)))
     cu = np.concatenate([[0], np.cumsum(lens)])
-    for i in pick:
+    worst = (0.0, 0.0)
+    for i in range(len(lens)):
         b, e = int(cu[i]), int(cu[i + 1])
         d = inputs.prefill_inputs(w, 0, b, e)
         ro, rf = oracle.prefill(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], [0, e - b], None)
-        assert_close(f"out seq {i} (len {e - b})", out[b:e], ro, w.dtype)
-        assert_close(f"final seq {i}", fin[i:i + 1], rf, w.dtype)
+        r1 = assert_close(f"out seq {i} (len {e - b})", out[b:e], ro, w.dtype)
+        r2 = assert_close(f"final seq {i}", fin[i:i + 1], rf, w.dtype)
+        worst = (max(worst[0], r1[0], r2[0]), max(worst[1], r1[1], r2[1]))
+    print(f"varlen, all {len(lens)} sequences: worst rel-L2 {worst[0]:.2e}, max-abs {worst[1]:.2e}")
 
 
 EDGE_LENS = [1, 15, 16, 17, 63, 64, 65, 0, 127, 128, 129, 200]
