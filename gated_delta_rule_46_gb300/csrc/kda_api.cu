@@ -31,6 +31,13 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
                                        void *workspace, size_t workspace_bytes, cudaStream_t st);
 int prefill_tc_launches(int64_t total, int num_seqs, int H, size_t workspace_bytes);
 void set_test_expire(int mask);
+size_t segment_map_workspace_bytes(int64_t total, int num_seqs, int H);
+cudaError_t launch_segment_map(const void *q, const void *k, const void *v, const void *z,
+                               const float *A, const float *beta, const int32_t *cu, int num_seqs,
+                               int64_t total, int H, float *M_out, float *b_out, void *workspace,
+                               size_t workspace_bytes, cudaStream_t st);
+cudaError_t launch_state_compose(const float *M, const float *b, int n_maps, int N, int H, int dk,
+                                 int dv, const float *init, float *states, cudaStream_t st);
 cudaError_t launch_state_slots(float *pool, int pool_size, const int32_t *slots, float *states,
                                int N, int H, int dk, int dv, bool to_pool, uint32_t *status,
                                cudaStream_t st);
@@ -233,6 +240,58 @@ kda_status_t kda_state_slots_copy(float *state_pool, int pool_size, const int32_
 }
 
 void kda_testing_expire_next_wait(int kernels) { kda::set_test_expire(kernels); }
+
+size_t kda_segment_map_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                      kda_dtype_t dtype) {
+    if (dtype != KDA_BF16 || dk != 128 || dv != 128 || num_seqs <= 0 || H <= 0 || total_tokens <= 0 ||
+        total_tokens >= (int64_t(1) << 31))
+        return (kda::kWsOrder + sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 0) + 255) & ~size_t(255);
+    return (kda::segment_map_workspace_bytes(total_tokens, num_seqs, H) + 255) & ~size_t(255);
+}
+
+kda_status_t kda_segment_map(const void *q, const void *k, const void *v, const void *z,
+                             const float *A, const float *beta, const int32_t *cu_seqlens,
+                             int num_seqs, int64_t total_tokens, int H, int dk, int dv,
+                             kda_dtype_t dtype, float *M, float *b, void *workspace,
+                             size_t workspace_bytes, kda_stream_t stream) {
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (dtype != KDA_BF16 || dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens >= (int64_t(1) << 31) || (int64_t)num_seqs * H >= (int64_t(1) << 31))
+        return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens || !A || !M || !b || !workspace || !aligned(workspace, 16)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (total_tokens == 0) {   // every map is the identity with no offset
+        if (workspace_bytes < 4) return KDA_ERR_INVALID_ARG;
+        if (cudaMemsetAsync(workspace, 0, 4, st) != cudaSuccess) return KDA_ERR_CUDA;
+        kda::ComposeParams ident{};
+        ident.init_identity = 1;
+        ident.out_last = M;
+        ident.last_prob = (int64_t)dk * dk;
+        ident.R = 0;
+        ident.ncols = dk;
+        if (kda::launch_compose(ident, num_seqs * H, dk, st) != cudaSuccess) return KDA_ERR_CUDA;
+        return from_cuda(cudaMemsetAsync(b, 0, sizeof(float) * (size_t)num_seqs * H * dk * dv, st));
+    }
+    if (!q || !k || !v || !z || !beta) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16)) return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < kda_segment_map_workspace_size(total_tokens, num_seqs, H, dk, dv, dtype))
+        return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_segment_map(q, k, v, z, A, beta, cu_seqlens, num_seqs, total_tokens, H, M,
+                                             b, workspace, workspace_bytes, st));
+}
+
+kda_status_t kda_state_compose(const float *M, const float *b, int n_maps, int num_seqs, int H, int dk,
+                               int dv, const float *initial_state, float *states, kda_stream_t stream) {
+    if (n_maps < 0 || num_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * H >= (int64_t(1) << 31)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    if (!states || (n_maps > 0 && (!M || !b))) return KDA_ERR_INVALID_ARG;
+    return from_cuda(kda::launch_state_compose(M, b, n_maps, num_seqs, H, dk, dv, initial_state, states,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
 
 kda_status_t kda_check_device_status(const void *workspace, kda_stream_t stream) {
     if (!workspace) return KDA_ERR_INVALID_ARG;

@@ -48,4 +48,30 @@ __device__ __forceinline__ void report_status(uint32_t *status, uint32_t code) {
     if (status) atomicCAS(status, kDevOk, code);
 }
 
+// Affine-map composition (kda_compose.cu): for P independent problems,
+// X_0 = init (or zeros, or the identity), X_{r+1} = M_r X_r + B_r, with
+// X [dk][ncols], M_r [dk][dk], B_r [dk][ncols] float32.
+struct ComposeParams {
+    const float *M;             // M_r of problem p at M + r m_step + p m_prob
+    int64_t m_step, m_prob;
+    const float *B;             // B_r of problem p at B + r b_step + p b_prob, or nullptr
+    int64_t b_step, b_prob;
+    const float *init;          // X_0 of problem p at init + p init_prob, or nullptr
+    int64_t init_prob;
+    int init_identity;          // with init == nullptr: X_0 = I (else zeros)
+    float *out_all;             // X_r of problem p at out_all + r out_step + p out_prob (r = 0..R), or nullptr
+    int64_t out_step, out_prob;
+    float *out_last;            // X_R of problem p at out_last + p last_prob, or nullptr
+    int64_t last_prob;
+    int R;                      // steps of every problem, unless cu_seqlens is given
+    int ncols;                  // columns of X (a multiple of 32)
+    // per-problem step counts of a segment map: problem p = (sequence p / H,
+    // head p % H) has ceil(ceil(len / 64) / seg_len) segments
+    const int32_t *cu_seqlens;
+    int H, seg_len;
+    int64_t total;
+    uint32_t *status;
+};
+cudaError_t launch_compose(const ComposeParams &p, int P, int dk, cudaStream_t st);
+
 }  // namespace kda

@@ -1105,6 +1105,11 @@ struct SplitParams {
     const float *diag;
     int64_t diag_stride;
     int test_expire;           // kExpire* bits (test support), 0 otherwise
+    // segment-map mode (kda_segment_map): every segment's map, the last one's
+    // too, as float32 S0 and M per (chain, segment) cell of MAP_CELL bytes;
+    // records then sit at the compact slots h rec_stride + (bos >> 6) + seq + c
+    uint8_t *map_out;
+    int64_t rec_stride;        // 0: records at chain W + (c - w0)
 };
 
 
@@ -1348,7 +1353,10 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const bool has_next = nit < n_items;
         const int nhx = has_next ? nxt.h * D : 0;
         const int nvalid = cur.nvalid;
-        uint8_t *rec = p.records + ((size_t)cur.chain * p.W + (cur.c - p.w0)) * REC_BYTES;
+        const size_t slot = p.rec_stride
+            ? (size_t)((int64_t)cur.h * p.rec_stride + ((cur.row0 - (int64_t)cur.c * C) >> 6) + cur.chain / H + cur.c)
+            : (size_t)cur.chain * p.W + (cur.c - p.w0);
+        uint8_t *rec = p.records + slot * REC_BYTES;
 
         if (tid < D) x.s_eAn[tid] = -expf(a_cur) * kLog2e;
         if (tid < C) x.s_beta[tid] = beta_cur;
@@ -1685,6 +1693,7 @@ constexpr uint32_t SMEM_SEG = SG_BAR + 128 + 1024;
 static_assert(SG_REC <= SG_STAGE && SMEM_SEG <= 232448, "segment kernel shared memory");
 constexpr uint32_t TG_S = 0, TG_M = 128, TG_U = 256, TG_UM = 320;   // TMEM columns
 constexpr size_t SEG_S0 = 0, SEG_MT = 65536, SEG_CELL = 98304;       // bytes per (chain, segment)
+constexpr size_t MAP_CELL = 2 * 65536;   // segment-map mode: float32 S0, then float32 M
 
 // M (held transposed in TMEM, lane m, column c -> M[c][m]) as the bf16 tile
 // B[c'][k] = M[c'][k] of the scan's MMA, written to global memory.
@@ -1761,7 +1770,8 @@ prefill_seg_kernel(const SplitParams p) {
     const int nchunks = (int)((eos - bos + C - 1) / C);
     const int c0 = sg * p.seg_len;
     const int c_end = (c0 + p.seg_len < nchunks) ? c0 + p.seg_len : nchunks;
-    if (c0 >= c_end || c_end >= nchunks) return;   // empty, or the last segment (nobody needs its map)
+    // empty, or the last segment of the scan plan (nobody needs its map there)
+    if (c0 >= c_end || (c_end >= nchunks && !p.map_out)) return;
 
     uint64_t *bar_never = bar_st + 7;   // test support: nothing arrives here
     if (tid == 0) {
@@ -1780,7 +1790,10 @@ prefill_seg_kernel(const SplitParams p) {
     const Ctx x = make_ctx(sm, tmem);
     ptx::pdl_wait();                 // the intra kernel's records
     ptx::pdl_launch_dependents();
-    const uint8_t *recs = p.records + (size_t)chain * p.W * REC_BYTES;
+    const size_t rec0 = p.rec_stride
+        ? (size_t)((int64_t)(chain % p.H) * p.rec_stride + (bos >> 6) + seq)
+        : (size_t)chain * p.W;
+    const uint8_t *recs = p.records + rec0 * REC_BYTES;
 
     uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
     uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
@@ -1849,9 +1862,15 @@ prefill_seg_kernel(const SplitParams p) {
         if (c + 2 < c_end) ++st_issued[k];
     }
     if (!*s_abort) {
-        uint8_t *cell = p.seg_out + ((size_t)chain * p.segs + sg) * SEG_CELL;
-        save_state(x, reinterpret_cast<float *>(cell + SEG_S0), TG_S);
-        save_m_tile(x, cell + SEG_MT, TG_M);
+        if (p.map_out) {   // float32 S0 [c][j] and M [c][c']
+            uint8_t *cell = p.map_out + ((size_t)chain * p.segs + sg) * MAP_CELL;
+            save_state(x, reinterpret_cast<float *>(cell), TG_S);
+            save_state(x, reinterpret_cast<float *>(cell + MAP_CELL / 2), TG_M);
+        } else {
+            uint8_t *cell = p.seg_out + ((size_t)chain * p.segs + sg) * SEG_CELL;
+            save_state(x, reinterpret_cast<float *>(cell + SEG_S0), TG_S);
+            save_m_tile(x, cell + SEG_MT, TG_M);
+        }
     }
     __syncthreads();
     if (*s_abort) {
@@ -2385,6 +2404,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
     sp.diag = reinterpret_cast<float *>(ws + ((scan.bytes + 255) & ~size_t(255)));
     sp.diag_stride = diag_stride(total, num_seqs);
     sp.test_expire = test_expire;
+    sp.map_out = nullptr; sp.rec_stride = 0;
     const int64_t items = chains * scan.max_chunks;
     if ((e = launch_diag_tiles(q, k, g, cu, total, num_seqs, H, const_cast<float *>(sp.diag), st)) != cudaSuccess)
         return e;
@@ -2402,6 +2422,121 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
                         tc::SMEM_SCAN, st, ms0, msin, sp)) != cudaSuccess)
         return e;
     return launch_pdl(tc::prefill_state_kernel, cells, tc::NT, tc::SMEM_STATE, st, mo, sp);
+}
+
+// ---- segment maps (kda_segment_map) ------------------------------------------
+// For every (sequence, head) the affine map of the whole sequence, S_out =
+// M S_in + b: the intra kernel writes the records of every chunk (at compact
+// slots, so a batch of many sequences needs no more than ~T/64 + N slots per
+// head), the segment kernel in its map mode runs every segment of every chain
+// from S = 0 and M = I in parallel and writes float32 (S0, M) per segment, and
+// two compositions fold each chain's segments in order: M = M_last ... M_0 and
+// b = the segments' S0 carried through the later maps.
+struct MapPlan {
+    bool ok;
+    int segs, seg_len;
+    int64_t max_chunks, stride;
+    size_t rec_off, cell_off, bytes;
+};
+
+static MapPlan plan_map(int64_t total, int num_seqs, int H) {
+    MapPlan m{};
+    const int64_t chains = (int64_t)num_seqs * H;
+    if (chains <= 0 || total <= 0) return m;
+    m.max_chunks = (total + tc::C - 1) / tc::C;
+    int64_t segs = sm_count() / chains;
+    segs = segs < 1 ? 1 : (segs > 64 ? 64 : segs);
+    int64_t len = (m.max_chunks + segs - 1) / segs;
+    if (len < 1) len = 1;
+    m.segs = (int)((m.max_chunks + len - 1) / len);
+    m.seg_len = (int)len;
+    m.stride = diag_stride(total, num_seqs);
+    m.rec_off = (kWsOrder + sizeof(int32_t) * (size_t)num_seqs + 1023) & ~size_t(1023);
+    m.cell_off = m.rec_off + (size_t)H * (size_t)m.stride * tc::REC_BYTES;
+    m.bytes = m.cell_off + (size_t)chains * (size_t)m.segs * tc::MAP_CELL;
+    m.ok = true;
+    return m;
+}
+
+size_t segment_map_workspace_bytes(int64_t total, int num_seqs, int H) {
+    const MapPlan m = plan_map(total, num_seqs, H);
+    return m.ok ? m.bytes : 0;
+}
+
+cudaError_t launch_segment_map(const void *q, const void *k, const void *v, const void *z,
+                               const float *A, const float *beta, const int32_t *cu, int num_seqs,
+                               int64_t total, int H, float *M_out, float *b_out, void *workspace,
+                               size_t workspace_bytes, cudaStream_t st) {
+    const MapPlan m = plan_map(total, num_seqs, H);
+    if (!m.ok) return cudaErrorInvalidValue;
+    if (workspace_bytes < m.bytes) return cudaErrorNotSupported;
+    CUtensorMap mq, mk, mv, mz;
+    if (!make_map(&mq, q, total, H) || !make_map(&mk, k, total, H) ||
+        !make_map(&mv, v, total, H) || !make_map(&mz, z, total, H))
+        return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws + kWsStatus);
+    cudaError_t e = launch_schedule(cu, num_seqs, reinterpret_cast<int32_t *>(ws + kWsOrder),
+                                    reinterpret_cast<uint32_t *>(ws + kWsCounter), status, st);
+    if (e != cudaSuccess) return e;
+    const void *kernels[2] = {(const void *)tc::prefill_intra_kernel<false>, (const void *)tc::prefill_seg_kernel};
+    const uint32_t smem[2] = {tc::SMEM_ALLOC, tc::SMEM_SEG};
+    for (int i = 0; i < 2; ++i)
+        if ((e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem[i])) != cudaSuccess)
+            return e;
+    const int sms = sm_count();
+    const int64_t chains = (int64_t)num_seqs * H;
+    tc::SplitParams sp{};
+    sp.A = A; sp.beta = beta; sp.cu_seqlens = cu; sp.initial_state = nullptr; sp.final_state = nullptr;
+    sp.out = nullptr;
+    sp.records = ws + m.rec_off;
+    sp.states = nullptr;
+    sp.status = status; sp.total_tokens = total; sp.num_seqs = num_seqs; sp.H = H;
+    sp.w0 = 0;
+    sp.wn = (int)m.max_chunks;
+    sp.W = (int)m.max_chunks;
+    sp.segs = 1;
+    sp.seg_len = m.seg_len;
+    sp.seg_out = nullptr; sp.seg_in = nullptr;
+    sp.diag = nullptr; sp.diag_stride = 0;
+    sp.test_expire = 0;
+    sp.map_out = ws + m.cell_off;
+    sp.rec_stride = m.stride;
+    const int64_t items = chains * m.max_chunks;
+    if ((e = launch_pdl(tc::prefill_intra_kernel<false>, (unsigned)(items < sms ? items : sms), tc::NT,
+                        tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
+        return e;
+    sp.segs = m.segs;
+    if ((e = launch_pdl(tc::prefill_seg_kernel, (unsigned)(chains * m.segs), tc::NT, tc::SMEM_SEG, st, sp)) !=
+        cudaSuccess)
+        return e;
+    // fold each chain's segments: M = M_last ... M_0 (from I), b (from 0, adding each S0)
+    const float *cells = reinterpret_cast<const float *>(ws + m.cell_off);
+    const int64_t cell_f = (int64_t)(tc::MAP_CELL / 4);
+    ComposeParams cp{};
+    cp.M = cells + cell_f / 2;
+    cp.m_step = cell_f;
+    cp.m_prob = (int64_t)m.segs * cell_f;
+    cp.B = nullptr;
+    cp.init = nullptr;
+    cp.init_identity = 1;
+    cp.out_all = nullptr;
+    cp.out_last = M_out;
+    cp.last_prob = (int64_t)tc::D * tc::D;
+    cp.ncols = tc::D;
+    cp.cu_seqlens = cu;
+    cp.H = H;
+    cp.seg_len = m.seg_len;
+    cp.total = total;
+    cp.status = status;
+    if ((e = launch_compose(cp, (int)chains, tc::D, st)) != cudaSuccess) return e;
+    cp.B = cells;
+    cp.b_step = cell_f;
+    cp.b_prob = (int64_t)m.segs * cell_f;
+    cp.init_identity = 0;
+    cp.out_last = b_out;
+    return launch_compose(cp, (int)chains, tc::D, st);
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
@@ -2447,6 +2582,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.seg_in = reinterpret_cast<float *>(ws + scan.seg_in_off);
         sp.diag = nullptr; sp.diag_stride = 0;
         sp.test_expire = test_expire;
+        sp.map_out = nullptr; sp.rec_stride = 0;
         const int64_t items = chains * scan.max_chunks;
         if ((e = launch_pdl(tc::prefill_intra_kernel<false>, (unsigned)(items < sms ? items : sms),
                             tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
@@ -2485,6 +2621,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.segs = 1; sp.seg_len = 0; sp.seg_out = nullptr; sp.seg_in = nullptr;
         sp.diag = nullptr; sp.diag_stride = 0;
         sp.test_expire = test_expire;
+        sp.map_out = nullptr; sp.rec_stride = 0;
         // fork: the side stream starts after everything already on `st`
         if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;

@@ -70,6 +70,12 @@ def lib():
             L.kda_prefill_kernel_launches.restype = I
             L.kda_check_device_status.argtypes = [P, P]
             L.kda_check_device_status.restype = I
+            L.kda_segment_map_workspace_size.argtypes = [I64, I, I, I, I, I]
+            L.kda_segment_map_workspace_size.restype = SZ
+            L.kda_segment_map.argtypes = [P, P, P, P, P, P, P, I, I64, I, I, I, I, P, P, P, SZ, P]
+            L.kda_segment_map.restype = I
+            L.kda_state_compose.argtypes = [P, P, I, I, I, I, I, P, P, P]
+            L.kda_state_compose.restype = I
             L.kda_testing_expire_next_wait.argtypes = [I]
             L.kda_testing_expire_next_wait.restype = None
             _lib = L
@@ -359,3 +365,66 @@ def testing_expire_next_wait(kernels: int) -> None:
     kernels named by the KDA_TESTING_* mask `kernels` see one bounded wait in
     their first CTA run out, and take their timeout path."""
     lib().kda_testing_expire_next_wait(int(kernels))
+
+
+def segment_map_workspace_size(total_tokens: int, num_seqs: int, H: int, dk: int, dv: int,
+                               dtype: torch.dtype = torch.bfloat16) -> int:
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib().kda_segment_map_workspace_size(total_tokens, num_seqs, H, dk, dv, code))
+
+
+def segment_map(q, k, v, z, A, beta, cu_seqlens, M=None, b=None, workspace=None, stream=None):
+    """The affine state map S_out = M S_in + b of every (sequence, head) of a
+    packed batch (kda_segment_map).  Returns (M [N, H, dk, dk], b [N, H, dk, dv])."""
+    _check(q, "q")
+    T, H, dk = q.shape
+    dv = v.shape[2] if v.dim() == 3 else -1
+    dev = q.device
+    for name, t in (("k", k), ("z", z)):
+        _check(t, name, (T, H, dk), q.dtype, dev)
+    _check(v, "v", (T, H, dv), q.dtype, dev)
+    _check(A, "A", (H, dk), torch.float32, dev)
+    _check(beta, "beta", (T, H), torch.float32, dev)
+    _check(cu_seqlens, "cu_seqlens", None, torch.int32, dev)
+    N = cu_seqlens.shape[0] - 1
+    if M is None:
+        M = torch.empty((N, H, dk, dk), dtype=torch.float32, device=dev)
+    if b is None:
+        b = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(M, "M", (N, H, dk, dk), torch.float32, dev)
+    _check(b, "b", (N, H, dk, dv), torch.float32, dev)
+    if workspace is None:
+        workspace = torch.empty(segment_map_workspace_size(T, N, H, dk, dv, q.dtype), dtype=torch.uint8,
+                                device=dev)
+    _check(workspace, "workspace", None, torch.uint8, dev)
+    with _on(dev):
+        st = lib().kda_segment_map(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                   _ptr(cu_seqlens), N, T, H, dk, dv, _dtype_code(q), _ptr(M), _ptr(b),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _raise(st, "kda_segment_map")
+    return M, b
+
+
+def state_compose(M, b, initial_state=None, states=None, stream=None):
+    """states[0] = initial_state (or zeros), states[r + 1] = M[r] states[r] + b[r]
+    (kda_state_compose).  M [R, N, H, dk, dk], b [R, N, H, dk, dv] f32; returns
+    states [R + 1, N, H, dk, dv]."""
+    _check(M, "M", None, torch.float32)
+    R, N, H, dk, dk2 = M.shape
+    if dk2 != dk:
+        raise ValueError("M must be [R, N, H, dk, dk]")
+    dev = M.device
+    _check(b, "b", None, torch.float32, dev)
+    if b.dim() != 5 or tuple(b.shape[:4]) != (R, N, H, dk):
+        raise ValueError(f"b must be [{R}, {N}, {H}, {dk}, dv], got {tuple(b.shape)}")
+    dv = b.shape[4]
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (N, H, dk, dv), torch.float32, dev)
+    if states is None:
+        states = torch.empty((R + 1, N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(states, "states", (R + 1, N, H, dk, dv), torch.float32, dev)
+    with _on(dev):
+        st = lib().kda_state_compose(_ptr(M), _ptr(b), R, N, H, dk, dv, _ptr(initial_state),
+                                     _ptr(states), _stream(stream))
+    _raise(st, "kda_state_compose")
+    return states

@@ -284,6 +284,63 @@ kda_status_t kda_state_slots_copy(float *state_pool, int pool_size, const int32_
                                   uint32_t *status, kda_stream_t stream);
 
 /*
+ * Context parallelism: one long sequence split over several workers ("Kimi K3
+ * internals analysis", section "3T급 MoE를 위한 인프라" (infrastructure for the
+ * 3T-class MoE), the KDA context-parallelism paragraph).  Over any segment of
+ * tokens the state map is affine,
+ *     S_out = M S_in + b,    M [dk, dk],  b [dk, dv]  (S rows = key channels),
+ * b being the segment run from a zero state and M the product of
+ * (I - beta_t k_t k_t^T) Diag(alpha_t) over its tokens t, the last on the left.  Each worker computes the map of
+ * its own segment (kda_segment_map), the workers exchange the maps (fixed size,
+ * whatever the segment length), each composes the maps of the segments before
+ * its own into its true incoming state (kda_state_compose) and runs its
+ * segment from that state (kda_chunk_prefill with initial_state).
+ *
+ * kda_segment_map -- for every sequence of a packed batch (each one a segment
+ * of some longer sequence) and every head, the map (M, b) of that sequence.
+ *   q, k, v, z, A, beta, cu_seqlens, num_seqs, total_tokens, H, dk, dv, dtype:
+ *                  as for kda_chunk_prefill; bf16 with dk = dv = 128 only
+ *                  (KDA_ERR_UNSUPPORTED otherwise), q/k/v/z 16-byte aligned
+ *   M              [num_seqs, H, dk, dk] float32 (written); I for an empty sequence
+ *   b              [num_seqs, H, dk, dv] float32 (written); 0 for an empty sequence
+ *   workspace      16-byte aligned, kda_segment_map_workspace_size() bytes:
+ *                  the status word (kda_check_device_status), the per-chunk
+ *                  records of every chunk (72.5 KB per 64-token chunk and head)
+ *                  and a 128 KB cell per (sequence, head, segment)
+ * Runs the chunk-parallel kernel of the prefill, the segment kernel in a mode
+ * that keeps float32 maps for every segment of every (sequence, head), and a
+ * float32 composition of each chain's segments in order.  The maps are meant
+ * for batches of a few long sequences (one per worker and head); M's columns
+ * are those of a state, so its rounding is that of a state carried through the
+ * bf16 tensor-core products of the prefill.
+ */
+size_t kda_segment_map_workspace_size(int64_t total_tokens, int num_seqs, int H, int dk, int dv,
+                                      kda_dtype_t dtype);
+kda_status_t kda_segment_map(const void *q, const void *k, const void *v, const void *z,
+                             const float *A, const float *beta, const int32_t *cu_seqlens,
+                             int num_seqs, int64_t total_tokens, int H, int dk, int dv,
+                             kda_dtype_t dtype, float *M, float *b, void *workspace,
+                             size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_state_compose -- composes affine state maps in order, for every
+ * (sequence, head): states[0] = initial_state (or zeros when NULL) and
+ *     states[r + 1] = M_r states[r] + b_r,   r = 0 .. n_maps - 1,
+ * so states[r] is the state with which segment r starts when segment 0
+ * starts from initial_state, and states[n_maps] the state after the last.
+ *   M              [n_maps, num_seqs, H, dk, dk] float32 (maps in segment order)
+ *   b              [n_maps, num_seqs, H, dk, dv] float32
+ *   initial_state  [num_seqs, H, dk, dv] float32, or NULL
+ *   states         [n_maps + 1, num_seqs, H, dk, dv] float32 (written)
+ * Plain float32 products (no tensor cores); n_maps = 0 copies the start state.
+ * All pointers are device pointers; M and b may be a gathered copy of other
+ * workers' maps, but must be in this device's memory.
+ */
+kda_status_t kda_state_compose(const float *M, const float *b, int n_maps, int num_seqs, int H,
+                               int dk, int dv, const float *initial_state, float *states,
+                               kda_stream_t stream);
+
+/*
  * kda_check_device_status -- synchronises `stream`, reads the status word that
  * kda_chunk_prefill (or kda_chunk_prefill_logdecay) keeps in `workspace`, and
  * returns the first device-side condition the last call recorded:

@@ -18,11 +18,12 @@ import oracle
 from gated_delta_rule_46_gb300 import (check_device_status, chunk_prefill,
                                        chunk_prefill_logdecay, gate, inputs,
                                        logdecay_workspace_size, prefill_kernel_launches,
-                                       testing_expire_next_wait, workspace_size)
+                                       workspace_size)
 from gated_delta_rule_46_gb300 import kda as K
 from gpu_util import assert_close, need_gpu, to_device
 
 KDA_ERR_DEVICE_TIMEOUT = K.KDA_ERR_DEVICE_TIMEOUT
+expire_next_wait = K.testing_expire_next_wait   # (a name pytest does not collect)
 
 pytestmark = pytest.mark.gpu
 
@@ -79,7 +80,7 @@ def test_expired_wait_is_reported_and_the_next_call_is_exact(plan, kernels):
     out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
     fin = torch.empty((N, H, 128, 128), dtype=torch.float32, device=dev)
 
-    testing_expire_next_wait(kernels)
+    expire_next_wait(kernels)
     chunk_prefill(*args, final_state=fin, out=out, workspace=ws)
     assert check_device_status(ws) == KDA_ERR_DEVICE_TIMEOUT
     torch.cuda.synchronize()                 # raises if the context had an error
@@ -103,7 +104,7 @@ def test_expired_wait_in_the_unbounded_decay_path(lens):
     gd = gate(g["z"], g["A"])
     ws = torch.zeros(logdecay_workspace_size(T, N, H, 128, 128), dtype=torch.uint8, device=dev)
     args = (g["q"], g["k"], g["v"], gd, g["beta"], g["cu_seqlens"], g["initial_state"])
-    testing_expire_next_wait(K.KDA_TESTING_FUSED | K.KDA_TESTING_INTRA | K.KDA_TESTING_STATE)
+    expire_next_wait(K.KDA_TESTING_FUSED | K.KDA_TESTING_INTRA | K.KDA_TESTING_STATE)
     out, fin = chunk_prefill_logdecay(*args, workspace=ws)
     assert check_device_status(ws) == KDA_ERR_DEVICE_TIMEOUT
     torch.cuda.synchronize()
@@ -123,7 +124,7 @@ def test_disarmed_mask_changes_nothing():
     args = (g["q"], g["k"], g["v"], g["z"], g["A"], g["beta"], g["cu_seqlens"], g["initial_state"])
     ws = torch.zeros(workspace_size(377, 2, 2, 128, 128), dtype=torch.uint8, device=dev)
     a = chunk_prefill(*args, workspace=ws)
-    testing_expire_next_wait(0)
+    expire_next_wait(0)
     b = chunk_prefill(*args, workspace=ws)
     assert check_device_status(ws) == 0
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
