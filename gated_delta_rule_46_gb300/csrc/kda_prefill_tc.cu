@@ -674,22 +674,27 @@ __device__ __forceinline__ void phase_rhs(const Ctx &x, uint32_t tm_ks, uint32_t
     st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg + 1), vt + 8);
 }
 
-// U^T into its bf16 operand tile, and S^T <- S^T Diag(2^G_end) in TMEM (the
-// dS MMA then accumulates onto it).
-__device__ __forceinline__ void phase_u_scale(const Ctx &x, uint32_t tm_u, uint32_t tm_s,
-                                              uint32_t off_ru, const float *gamma) {
-    float U[16], Sx[32], gm[32];
-    ptx::tmem_ld16(x.lane_base + tm_u + 16 * x.cg, U);
+// S^T <- S^T Diag(2^G_end) in TMEM (the dS MMA then accumulates onto it).  It
+// touches only the master state, so it can run while an MMA that does not
+// write the master (the U product) is in flight.
+__device__ __forceinline__ void scale_state(const Ctx &x, uint32_t tm_s, const float *gamma) {
+    float Sx[32], gm[32];
     ptx::tmem_ld32(x.lane_base + tm_s + 32 * x.cg, Sx);
     const float *g = gamma + 32 * x.cg;
     ld8(g, gm); ld8(g + 8, gm + 8); ld8(g + 16, gm + 16); ld8(g + 24, gm + 24);
     ptx::tmem_ld_wait();
-    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg), U);
-    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg + 1), U + 8);
 #pragma unroll
     for (int i = 0; i < 32; ++i) Sx[i] *= gm[i];
     ptx::tmem_st32(x.lane_base + tm_s + 32 * x.cg, Sx);
     ptx::tmem_st_wait();
+}
+// U^T out of TMEM into its bf16 operand tile.
+__device__ __forceinline__ void u_out(const Ctx &x, uint32_t tm_u, uint32_t off_ru) {
+    float U[16];
+    ptx::tmem_ld16(x.lane_base + tm_u + 16 * x.cg, U);
+    ptx::tmem_ld_wait();
+    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg), U);
+    st_chunk(x.sm + off_ru, swz(x.ch, 2 * x.cg + 1), U + 8);
 }
 
 // New state's bf16 copy into the state operand tile; O^T out of TMEM into the
@@ -961,14 +966,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             ptx::tc_fence_after_sync();
             phase_extract_PL(x, OFF_PB, UNB ? reinterpret_cast<const float *>(sm + OFF_DG) : nullptr);
             __syncthreads();
-            phase_diag(x);
+            // warps 0-3: the diagonal blocks of the inverse; warps 8-15 meanwhile the
+            // RHS, once the state MMA (reading B1, where RHS goes) has completed
+            if (warp < 4) {
+                phase_diag(x);
+            } else if (warp >= 8) {
+                if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
+                ptx::tc_fence_after_sync();
+                phase_rhs_w8(x, TM_D1, OFF_VT, OFF_RU);
+            }
             __syncthreads();
             if (tid == 0 && has_next) tma_2box(sm + OFF_V, &tm_v, hx, (int)next_row, bar_v);
             if (has_next) ++v_issued;
-            // the state MMA (still reading B1, where T and RHS go) overlapped the diagonal solve
-            if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
+            if (warp < 8) {   // (warps 8-15 have waited already)
+                if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
+            }
             ptx::tc_fence_after_sync();
-            solve_T(x, OFF_TB, true, TM_D1, OFF_VT, OFF_RU);
+            solve_T(x, OFF_TB, false, TM_D1, OFF_VT, OFF_RU);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -990,10 +1004,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (next_row + tid < eos) beta_next = p.beta[(next_row + tid) * H + h];
             }
 
+            // S^T <- S^T Diag(2^G_end) while the U MMA runs (it does not touch the master)
+            scale_state(x, TM_D3, x.s_gamma);
+
             // =============================== phase C: U^T to smem, output and state MMAs
             if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            phase_u_scale(x, TM_D2, TM_D3, OFF_RU, x.s_gamma);
+            u_out(x, TM_D2, OFF_RU);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -1607,9 +1624,11 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         }
         ++s_issued;
         __syncthreads();
+        // the master state is not touched by that MMA: scale it meanwhile
+        scale_state(x, TS_D3, reinterpret_cast<const float *>(stg + REC_G));
         if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
-        phase_u_scale(x, d1, TS_D3, SB_RU, reinterpret_cast<const float *>(stg + REC_G));
+        u_out(x, d1, SB_RU);
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
@@ -1827,11 +1846,14 @@ prefill_seg_kernel(const SplitParams p) {
             ptx::mma_commit(bar_s);
         }
         ++s_issued;
+        // the two master states are not touched by those MMAs: scale them meanwhile
+        const float *gamma = reinterpret_cast<const float *>(stg + SG_G);
+        scale_state(x, TG_S, gamma);
+        scale_state(x, TG_M, gamma);
         if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
-        const float *gamma = reinterpret_cast<const float *>(stg + SG_G);
-        phase_u_scale(x, TG_U, TG_S, SG_RU, gamma);
-        phase_u_scale(x, TG_UM, TG_M, SG_RUM, gamma);
+        u_out(x, TG_U, SG_RU);
+        u_out(x, TG_UM, SG_RUM);
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
