@@ -92,7 +92,9 @@ constexpr uint32_t OFF_HT = OFF_EAN + 512;           // [8][128]: half-tile sums
 constexpr uint32_t OFF_GAMMA = OFF_HT + 4096;        // 128 float: 2^(G_end)
 constexpr uint32_t OFF_BAR = OFF_GAMMA + 512;        // mbarriers
 constexpr uint32_t OFF_SLOT = OFF_BAR + 64;          // TMEM base, work item, abort flag
-constexpr uint32_t SMEM_USED = OFF_SLOT + 64;
+constexpr uint32_t OFF_CU = OFF_SLOT + 64;           // intra kernel: cu_seqlens cache (CU_CACHE entries)
+constexpr int CU_CACHE = 256;
+constexpr uint32_t SMEM_USED = OFF_CU + 4 * CU_CACHE;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // slack to align the base to 1024 B
 static_assert(OFF_GB + 2 * GB_KBLK <= OFF_B1, "right-factor tiles overlap");
 static_assert(OFF_Y + 64 * LSTR * 4 <= OFF_TB, "solve scratch overlaps");
@@ -779,6 +781,22 @@ __device__ __forceinline__ void bulk_load(uint8_t *sdst, const uint8_t *gsrc, ui
         : "memory");
 }
 
+// The same copies with an L2 cache policy.
+__device__ __forceinline__ void bulk_store_hint(uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(ptx::smem_addr(ssrc)), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_copy_in_hint(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
+                                                  uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            ptx::smem_addr(sdst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
 // Slot of chunk c of sequence seq (first token bos), head h, in the diagonal-tile
 // store of the unbounded mode (see diag_tiles_kernel).
 __host__ __device__ __forceinline__ int64_t diag_slot(int64_t stride, int h, int64_t bos, int seq, int c) {
@@ -816,6 +834,22 @@ __device__ __forceinline__ void tma_2box(uint8_t *dst, const CUtensorMap *tm, in
     ptx::mbar_arrive_expect_tx(bar, 16384);
     ptx::tma_load_2d(dst, tm, hx, y, bar);
     ptx::tma_load_2d(dst + 8192, tm, hx + 64, y, bar);
+}
+// The same with an L2 cache policy (the chunk-parallel kernel reads its inputs
+// with evict_first, so that the per-chunk records it writes stay in L2).
+__device__ __forceinline__ void tma_qk_h(uint8_t *sm, const CUtensorMap *tq, const CUtensorMap *tk,
+                                         int hx, int y, uint64_t *bar, uint64_t pol) {
+    ptx::mbar_arrive_expect_tx(bar, 32768);
+    ptx::tma_load_2d_hint(sm + OFF_QK, tq, hx, y, bar, pol);
+    ptx::tma_load_2d_hint(sm + OFF_QK + 8192, tk, hx, y, bar, pol);
+    ptx::tma_load_2d_hint(sm + OFF_QK + 16384, tq, hx + 64, y, bar, pol);
+    ptx::tma_load_2d_hint(sm + OFF_QK + 24576, tk, hx + 64, y, bar, pol);
+}
+__device__ __forceinline__ void tma_2box_h(uint8_t *dst, const CUtensorMap *tm, int hx, int y,
+                                           uint64_t *bar, uint64_t pol) {
+    ptx::mbar_arrive_expect_tx(bar, 16384);
+    ptx::tma_load_2d_hint(dst, tm, hx, y, bar, pol);
+    ptx::tma_load_2d_hint(dst + 8192, tm, hx + 64, y, bar, pol);
 }
 
 // Fused kernel: one CTA per SM, persistent over (sequence, head) chains taken
@@ -1127,6 +1161,9 @@ struct SplitParams {
     // records then sit at the compact slots h rec_stride + (bos >> 6) + seq + c
     uint8_t *map_out;
     int64_t rec_stride;        // 0: records at chain W + (c - w0)
+    // the records of the whole call fit in L2: they are written and read with
+    // an evict-last policy, and the state pass drops them from L2 after use
+    int rec_in_l2;
 };
 
 
@@ -1138,11 +1175,11 @@ struct ItemInfo {
 
 // Work item `it` of a window: chain it / wn, chunk w0 + it % wn; false when
 // that chunk lies past the end of its sequence.
-__device__ __forceinline__ bool item_info(const SplitParams &p, int it, ItemInfo &r) {
+__device__ __forceinline__ bool item_info(const SplitParams &p, const int32_t *cu, int it, ItemInfo &r) {
     const int chain = it / p.wn;
     const int c = p.w0 + it % p.wn;
     const int seq = chain / p.H;
-    int64_t bos = p.cu_seqlens[seq], eos = p.cu_seqlens[seq + 1];
+    int64_t bos = cu[seq], eos = cu[seq + 1];
     if (bos < 0 || eos < bos || eos > p.total_tokens) return false;
     const int64_t row0 = bos + (int64_t)c * C;
     if (row0 >= eos) return false;
@@ -1315,6 +1352,15 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ptx::fence_mbar_init();
         *s_abort = 0;
     }
+    // the sequence offsets, read once into shared memory when they fit (the
+    // next item's bounds are then not a global-memory round trip on every
+    // item's critical path); the inputs were complete before the previous
+    // kernel of the call started, so this may precede the dependency wait
+    int32_t *s_cu = reinterpret_cast<int32_t *>(sm + OFF_CU);
+    const bool cu_cached = p.num_seqs < CU_CACHE;
+    if (cu_cached)
+        for (int i = tid; i <= p.num_seqs; i += NT) s_cu[i] = p.cu_seqlens[i];
+    const int32_t *cu = cu_cached ? s_cu : p.cu_seqlens;
     if (warp == 0) {
         ptx::tmem_alloc(s_tmem, 256);
         ptx::tmem_relinquish();
@@ -1327,18 +1373,39 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
     uint32_t g_issued = 0, g_done = 0, d_issued = 0, d_done = 0;
+    // inputs are read once (evict first); the records are read back by the next
+    // kernels of the call (evict last), and the last reader discards them
+    // (only when the records of the call fit in L2; plain copies otherwise)
+    const bool hint = p.rec_in_l2 != 0;
+    const uint64_t pol_in = ptx::policy_evict_first(), pol_rec = ptx::policy_evict_last();
+    auto load_qk = [&](int hx, int row) {
+        if (hint) tma_qk_h(sm, &tm_q, &tm_k, hx, row, bar_qk, pol_in);
+        else tma_qk(sm, &tm_q, &tm_k, hx, row, bar_qk);
+    };
+    auto load_v = [&](int hx, int row) {
+        if (hint) tma_2box_h(sm + OFF_V, &tm_v, hx, row, bar_v, pol_in);
+        else tma_2box(sm + OFF_V, &tm_v, hx, row, bar_v);
+    };
+    auto export_rec = [&](uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes) {
+        if (hint) bulk_store_hint(gdst, ssrc, bytes, pol_rec);
+        else bulk_store(gdst, ssrc, bytes);
+    };
     auto load_gz = [&](int hx, int row) {   // z tile, or the four g boxes
         if (UNB) {
             ptx::mbar_arrive_expect_tx(bar_z, 32768);
-            for (int b = 0; b < 4; ++b) ptx::tma_load_2d(sm + g_box_off<true>(b), &tm_z, hx + 32 * b, row, bar_z);
+            for (int b = 0; b < 4; ++b) {
+                if (hint) ptx::tma_load_2d_hint(sm + g_box_off<true>(b), &tm_z, hx + 32 * b, row, bar_z, pol_in);
+                else ptx::tma_load_2d(sm + g_box_off<true>(b), &tm_z, hx + 32 * b, row, bar_z);
+            }
         } else {
-            tma_2box(sm + OFF_Z, &tm_z, hx, row, bar_z);
+            if (hint) tma_2box_h(sm + OFF_Z, &tm_z, hx, row, bar_z, pol_in);
+            else tma_2box(sm + OFF_Z, &tm_z, hx, row, bar_z);
         }
     };
     const int n_items = p.num_seqs * H * p.wn;
     ItemInfo cur, nxt;
     int it = blockIdx.x;
-    while (it < n_items && !item_info(p, it, cur)) it += gridDim.x;
+    while (it < n_items && !item_info(p, cu, it, cur)) it += gridDim.x;
     // this thread's entry of A and beta for the coming item, raw: loaded one item
     // ahead and not used until that item starts, so the load latency is hidden
     float a_cur = 0.f, beta_cur = 0.f;
@@ -1350,9 +1417,9 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (tid < cur.nvalid) beta_cur = p.beta[(cur.row0 + tid) * H + cur.h];
         if (tid == 0) {
             const int hx = cur.h * D;
-            tma_qk(sm, &tm_q, &tm_k, hx, (int)cur.row0, bar_qk);
+            load_qk(hx, (int)cur.row0);
             load_gz(hx, (int)cur.row0);
-            tma_2box(sm + OFF_V, &tm_v, hx, (int)cur.row0, bar_v);
+            load_v(hx, (int)cur.row0);
         }
         ++qk_issued; ++z_issued; ++v_issued;
     }
@@ -1366,7 +1433,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     bool first_item = true;
     while (it < n_items) {
         int nit = it + gridDim.x;
-        while (nit < n_items && !item_info(p, nit, nxt)) nit += gridDim.x;
+        while (nit < n_items && !item_info(p, cu, nit, nxt)) nit += gridDim.x;
         const bool has_next = nit < n_items;
         const int nhx = has_next ? nxt.h * D : 0;
         const int nvalid = cur.nvalid;
@@ -1406,10 +1473,10 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             mma_k<8>(tmem + TM_G, sbase + OFF_QK, 16384u, sbase + OFF_GB, GB_KBLK,
                      ptx::idesc_bf16_f32(128, 160), false);
             ptx::mma_commit(bar_g);
-            bulk_store(rec + REC_KE, sm + OFF_KE, 16384);
-            bulk_store(rec + REC_G, reinterpret_cast<const uint8_t *>(x.s_gamma), 512);
-            bulk_store(rec + REC_B1 + 8192, sm + OFF_B1 + 8192, 8192);                 // Q~, K-block 0
-            bulk_store(rec + REC_B1 + 16384 + 8192, sm + OFF_B1 + 16384 + 8192, 8192); // Q~, K-block 1
+            export_rec(rec + REC_KE, sm + OFF_KE, 16384);
+            export_rec(rec + REC_G, reinterpret_cast<const uint8_t *>(x.s_gamma), 512);
+            export_rec(rec + REC_B1 + 8192, sm + OFF_B1 + 8192, 8192);                 // Q~, K-block 0
+            export_rec(rec + REC_B1 + 16384 + 8192, sm + OFF_B1 + 16384 + 8192, 8192); // Q~, K-block 1
             ptx::bulk_commit();
         }
         ++g_issued;
@@ -1419,7 +1486,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         phase_vt(x, nvalid);
 
         if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
-        if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, nhx, (int)nxt.row0, bar_qk);
+        if (tid == 0 && has_next) load_qk(nhx, (int)nxt.row0);
         if (has_next) ++qk_issued;
         if (UNB) {
             if (ptx::mbar_wait(bar_d, d_done & 1, kWaitBudget)) ++d_done; else *s_abort = 1;
@@ -1431,8 +1498,8 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         phase_diag(x);
         __syncthreads();
         if (tid == 0) {
-            if (has_next) tma_2box(sm + OFF_V, &tm_v, nhx, (int)nxt.row0, bar_v);
-            bulk_store(rec + REC_PB, sm + OFF_PB, 8192);
+            if (has_next) load_v(nhx, (int)nxt.row0);
+            export_rec(rec + REC_PB, sm + OFF_PB, 8192);
             ptx::bulk_commit();
         }
         if (has_next) ++v_issued;
@@ -1461,9 +1528,9 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __syncthreads();
         if (*s_abort) break;
         if (tid == 0) {
-            bulk_store(rec + REC_B1, sm + OFF_NW_INTRA, 8192);                  // -W, K-block 0
-            bulk_store(rec + REC_B1 + 16384, sm + OFF_NW_INTRA + 8192, 8192);   // -W, K-block 1
-            bulk_store(rec + REC_UT, sm + OFF_UT_INTRA, 16384);
+            export_rec(rec + REC_B1, sm + OFF_NW_INTRA, 8192);                  // -W, K-block 0
+            export_rec(rec + REC_B1 + 16384, sm + OFF_NW_INTRA + 8192, 8192);   // -W, K-block 1
+            export_rec(rec + REC_UT, sm + OFF_UT_INTRA, 16384);
             ptx::bulk_commit();
         }
         it = nit;
@@ -1584,21 +1651,37 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     ptx::pdl_wait();                 // records, incoming states of the previous kernels
     ptx::pdl_launch_dependents();
     const uint8_t *recs = p.records + (size_t)chain * p.W * REC_BYTES;
+    // this kernel is the last reader of the records: they are fetched with
+    // evict_first and, once in shared memory, dropped from L2 without a write-back
+    const uint64_t pol_rec = ptx::policy_evict_first();
+    auto fetch = [&](int k, int c) {
+        const uint8_t *r = recs + (size_t)(c - rec_c0) * REC_BYTES;
+        if (p.rec_in_l2) {
+            ptx::mbar_arrive_expect_tx(bar_st + k, REC_BYTES);
+            bulk_copy_in_hint(sm + k * SB_STAGE, r, REC_BYTES, bar_st + k, pol_rec);
+        } else {
+            bulk_load(sm + k * SB_STAGE, r, REC_BYTES, bar_st + k);
+        }
+    };
+    auto discard = [&](int c) {
+        if (!p.rec_in_l2) return;
+        const uint8_t *r = recs + (size_t)(c - rec_c0) * REC_BYTES;
+        for (int i = tid; i < (int)(REC_BYTES / 128); i += NT) ptx::discard_l2(r + (size_t)i * 128);
+    };
 
     uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
     uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
     const int c0 = w0;
     if (tid == 0) {
         for (int k = 0; k < 2; ++k)
-            if (c0 + k < c_end)
-                bulk_load(sm + k * SB_STAGE, recs + (size_t)(c0 + k - rec_c0) * REC_BYTES, REC_BYTES, bar_st + k);
+            if (c0 + k < c_end) fetch(k, c0 + k);
     }
     for (int k = 0; k < 2; ++k)
         if (c0 + k < c_end) ++st_issued[k];
     const float *src = first ? (p.initial_state ? p.initial_state + sidx : nullptr) : carried;
     load_state(x, src, TS_D3, SB_ST);
     if (c0 < c_end) {
-        if (ptx::mbar_wait(bar_st, st_done[0] & 1, kWaitBudget)) ++st_done[0]; else *s_abort = 1;
+        if (ptx::mbar_wait(bar_st, st_done[0] & 1, kWaitBudget)) { ++st_done[0]; discard(c0); } else *s_abort = 1;
         preload_u(x, TS_D1, sm + REC_UT);
     }
     if (test_wait_expires(p.test_expire, kExpireState, bar_never)) *s_abort = 1;
@@ -1643,8 +1726,12 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         ++m_issued;
         // meanwhile: the next chunk's [U~ | 0] into the other D1 buffer
         if (c + 1 < c_end) {
-            if (ptx::mbar_wait(bar_st + (k ^ 1), st_done[k ^ 1] & 1, kWaitBudget)) ++st_done[k ^ 1];
-            else *s_abort = 1;
+            if (ptx::mbar_wait(bar_st + (k ^ 1), st_done[k ^ 1] & 1, kWaitBudget)) {
+                ++st_done[k ^ 1];
+                discard(c + 1);
+            } else {
+                *s_abort = 1;
+            }
             preload_u(x, TS_D1 + 128 * (k ^ 1), sm + (k ^ 1) * SB_STAGE + REC_UT);
         }
         if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
@@ -1656,8 +1743,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         if (*s_abort) break;
         store_output(x, &tm_o, SB_RU, p.out, row0, nvalid, hx, rowstride);
         // stage k has been consumed: fetch the record two chunks ahead into it
-        if (tid == 0 && c + 2 < c_end)
-            bulk_load(stg, recs + (size_t)(c + 2 - rec_c0) * REC_BYTES, REC_BYTES, bar_st + k);
+        if (tid == 0 && c + 2 < c_end) fetch(k, c + 2);
         if (c + 2 < c_end) ++st_issued[k];
     }
     if (!*s_abort) {
@@ -1728,13 +1814,19 @@ __device__ __forceinline__ void save_m_tile(const Ctx &x, uint8_t *dst, uint32_t
         *reinterpret_cast<__nv_bfloat16 *>(kb + swz(32 * x.cg + i, mc) + mo) = __float2bfloat16_rn(X[i]);
 }
 
-__device__ __forceinline__ void load_stage_seg(uint8_t *stg, const uint8_t *rec, uint64_t *bar) {
+// (the records are read again by the state pass: when they fit, their lines
+// are kept in L2)
+__device__ __forceinline__ void load_stage_seg(uint8_t *stg, const uint8_t *rec, uint64_t *bar, bool keep) {
     ptx::mbar_arrive_expect_tx(bar, SG_REC);
-    bulk_copy_in(stg + SG_NW, rec + REC_B1, 8192, bar);
-    bulk_copy_in(stg + SG_NW + 8192, rec + REC_B1 + 16384, 8192, bar);
-    bulk_copy_in(stg + SG_KE, rec + REC_KE, 16384, bar);
-    bulk_copy_in(stg + SG_UT, rec + REC_UT, 16384, bar);
-    bulk_copy_in(stg + SG_G, rec + REC_G, 512, bar);
+    const uint32_t dst[5] = {SG_NW, SG_NW + 8192, SG_KE, SG_UT, SG_G};
+    const uint32_t src[5] = {REC_B1, REC_B1 + 16384, REC_KE, REC_UT, REC_G};
+    const uint32_t len[5] = {8192, 8192, 16384, 16384, 512};
+    const uint64_t pol = ptx::policy_evict_last();
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        if (keep) bulk_copy_in_hint(stg + dst[i], rec + src[i], len[i], bar, pol);
+        else bulk_copy_in(stg + dst[i], rec + src[i], len[i], bar);
+    }
 }
 
 // The identity as a transposed state: TMEM float32 and its bf16 operand copy.
@@ -1818,7 +1910,7 @@ prefill_seg_kernel(const SplitParams p) {
     uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
     if (tid == 0) {
         for (int k = 0; k < 2; ++k)
-            if (c0 + k < c_end) load_stage_seg(sm + k * SG_STAGE, recs + (size_t)(c0 + k) * REC_BYTES, bar_st + k);
+            if (c0 + k < c_end) load_stage_seg(sm + k * SG_STAGE, recs + (size_t)(c0 + k) * REC_BYTES, bar_st + k, p.rec_in_l2);
     }
     for (int k = 0; k < 2; ++k)
         if (c0 + k < c_end) ++st_issued[k];
@@ -1880,7 +1972,7 @@ prefill_seg_kernel(const SplitParams p) {
         __syncthreads();
         if (*s_abort) break;
         if (tid == 0 && c + 2 < c_end)
-            load_stage_seg(stg, recs + (size_t)(c + 2) * REC_BYTES, bar_st + k);
+            load_stage_seg(stg, recs + (size_t)(c + 2) * REC_BYTES, bar_st + k, p.rec_in_l2);
         if (c + 2 < c_end) ++st_issued[k];
     }
     if (!*s_abort) {
@@ -2172,6 +2264,17 @@ static bool make_map(CUtensorMap *m, const void *base, int64_t T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Bytes of L2 on the current device.
+static size_t l2_bytes() {
+    int dev = 0, b = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&b, cudaDevAttrL2CacheSize, dev);
+    return (size_t)b;
+}
+// Whether `bytes` of per-chunk records can stay in L2 beside the streamed
+// inputs (at most three quarters of it).
+static int records_fit_l2(size_t bytes) { return bytes <= l2_bytes() / 4 * 3 ? 1 : 0; }
+
 static int sm_count() {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -2427,6 +2530,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
     sp.diag_stride = diag_stride(total, num_seqs);
     sp.test_expire = test_expire;
     sp.map_out = nullptr; sp.rec_stride = 0;
+    sp.rec_in_l2 = records_fit_l2((size_t)chains * scan.max_chunks * tc::REC_BYTES);
     const int64_t items = chains * scan.max_chunks;
     if ((e = launch_diag_tiles(q, k, g, cu, total, num_seqs, H, const_cast<float *>(sp.diag), st)) != cudaSuccess)
         return e;
@@ -2525,6 +2629,7 @@ cudaError_t launch_segment_map(const void *q, const void *k, const void *v, cons
     sp.test_expire = 0;
     sp.map_out = ws + m.cell_off;
     sp.rec_stride = m.stride;
+    sp.rec_in_l2 = records_fit_l2((size_t)H * (size_t)m.stride * tc::REC_BYTES);   // (kept for the segment kernel)
     const int64_t items = chains * m.max_chunks;
     if ((e = launch_pdl(tc::prefill_intra_kernel<false>, (unsigned)(items < sms ? items : sms), tc::NT,
                         tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
@@ -2605,6 +2710,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.diag = nullptr; sp.diag_stride = 0;
         sp.test_expire = test_expire;
         sp.map_out = nullptr; sp.rec_stride = 0;
+        sp.rec_in_l2 = records_fit_l2((size_t)chains * scan.max_chunks * tc::REC_BYTES);
         const int64_t items = chains * scan.max_chunks;
         if ((e = launch_pdl(tc::prefill_intra_kernel<false>, (unsigned)(items < sms ? items : sms),
                             tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz, sp)) != cudaSuccess)
@@ -2644,6 +2750,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         sp.diag = nullptr; sp.diag_stride = 0;
         sp.test_expire = test_expire;
         sp.map_out = nullptr; sp.rec_stride = 0;
+        sp.rec_in_l2 = records_fit_l2(2 * plan.window_bytes);
         // fork: the side stream starts after everything already on `st`
         if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
