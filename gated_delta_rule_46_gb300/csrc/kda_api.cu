@@ -23,6 +23,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
                               void *out, void *workspace, size_t workspace_bytes, cudaStream_t st);
+cudaError_t launch_prefill_chunk_simt(const void *q, const void *k, const void *v, const void *z,
+                                      const float *A, const float *beta, const int32_t *cu, int num_seqs,
+                                      int64_t total, int H, int dk, int dv, bool bf16, const float *s0,
+                                      float *s1, void *out, uint32_t *status, cudaStream_t st);
 size_t prefill_tc_workspace_bytes(int64_t total, int num_seqs, int H);
 size_t prefill_tc_logdecay_workspace_bytes(int64_t total, int num_seqs, int H);
 cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void *v, const float *g,
@@ -152,12 +156,14 @@ kda_status_t kda_chunk_prefill(const void *q, const void *k, const void *v, cons
                                                 total_tokens, H, initial_state, final_state, out,
                                                 workspace, workspace_bytes, st));
     }
+    // float32 inputs, dk or dv of 32 or 64 (or unaligned buffers): the chunkwise
+    // algebra in float32 on the CUDA cores
     uint32_t *status = reinterpret_cast<uint32_t *>(ws + kda::kWsStatus);
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), st);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    return from_cuda(kda::launch_prefill_serial(q, k, v, z, A, beta, cu_seqlens, num_seqs,
-                                                total_tokens, H, dk, dv, dtype == KDA_BF16,
-                                                initial_state, final_state, out, status, st));
+    return from_cuda(kda::launch_prefill_chunk_simt(q, k, v, z, A, beta, cu_seqlens, num_seqs,
+                                                    total_tokens, H, dk, dv, dtype == KDA_BF16,
+                                                    initial_state, final_state, out, status, st));
 }
 
 kda_status_t kda_chunk_prefill_logdecay(const void *q, const void *k, const void *v,

@@ -18,11 +18,10 @@
 #include "kda_common.cuh"
 
 namespace kda {
-cudaError_t launch_prefill_serial(const void *q, const void *k, const void *v, const void *z,
-                                  const float *A, const float *beta, const int32_t *cu,
-                                  int num_seqs, int64_t total, int H, int dk, int dv, bool bf16,
-                                  const float *s0, float *s1, void *out, uint32_t *status,
-                                  cudaStream_t st, const float *g = nullptr);
+cudaError_t launch_prefill_chunk_simt(const void *q, const void *k, const void *v, const void *z,
+                                      const float *A, const float *beta, const int32_t *cu, int num_seqs,
+                                      int64_t total, int H, int dk, int dv, bool bf16, const float *s0,
+                                      float *s1, void *out, uint32_t *status, cudaStream_t st);
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *z,
                               const float *A, const float *beta, const int32_t *cu,
                               int num_seqs, int64_t total, int H, const float *s0, float *s1,
@@ -104,9 +103,9 @@ extern "C" kda_status_t kda_chunk_prefill_noalloc(
     }
     uint32_t *status = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(scratch) + kda::kWsStatus);
     if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return KDA_ERR_CUDA;
-    return kda::launch_prefill_serial(q, k, v, z, A, beta, cu_seqlens, num_seqs, total_tokens, H,
-                                      dk, dv, dtype == KDA_BF16, initial_state, final_state, out,
-                                      status, st) == cudaSuccess
+    return kda::launch_prefill_chunk_simt(q, k, v, z, A, beta, cu_seqlens, num_seqs, total_tokens, H,
+                                          dk, dv, dtype == KDA_BF16, initial_state, final_state, out,
+                                          status, st) == cudaSuccess
                ? KDA_OK
                : KDA_ERR_CUDA;
 }

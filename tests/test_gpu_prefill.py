@@ -87,6 +87,25 @@ def test_edge_lengths_all_head_sizes(dtype, dk, dv, init):
         assert torch.count_nonzero(fin[EDGE_LENS.index(0)]) == 0
 
 
+@pytest.mark.parametrize("dtype,dk,dv,slow", [(torch.float32, 128, 128, False), (torch.float32, 128, 128, True),
+                                              (torch.float32, 32, 64, True), (torch.bfloat16, 64, 32, True),
+                                              (torch.bfloat16, 32, 128, False)])
+def test_chunked_float32_path_long_sequences(dtype, dk, dv, slow):
+    """The chunkwise float32 kernel (float32 inputs, head sizes 32 and 64) over
+    sequences of many 16-token chunks, the state carried from chunk to chunk;
+    with gates near 0 (z shifted down by 10) the carried state dominates the
+    outputs.  Tolerance 1e-4 for float32, the bf16 one otherwise."""
+    dev = need_gpu()
+    w = inputs.custom([1200, 301, 16], H=2, dk=dk, dv=dv, dtype=dtype, init="randn0.1", wid=17)
+    d = inputs.prefill_inputs(w)
+    if slow:
+        d["z"] = (d["z"].float() - 10.0).to(dtype)
+    out, fin = _run_gpu(d, dev)
+    ro, rf = _run_oracle(d)
+    assert_close("out", out, ro, dtype)
+    assert_close("final state", fin, rf, dtype)
+
+
 def test_null_final_state_and_in_place_state():
     dev = need_gpu()
     w = inputs.custom([300, 77], H=2, dk=128, dv=128, dtype=torch.bfloat16, init="randn0.1", wid=12)
