@@ -441,6 +441,14 @@ def run_gpu(args):
         # the varlen batch through the unbounded-decay path (fused kernel, unbounded mode)
         ablation["varlen"] = _time_large_prefill(kda, inputs, 2, dev, seed, flush, barrier, agg_max,
                                                  peak, peak_kind, unbounded=True)
+        # the 4096-token layer in float32 and with 64-channel heads (the chunkwise
+        # float32 kernel on the CUDA cores)
+        for case in ("prefill-f32", "prefill-d64"):
+            name, lens, H = CASES[case]
+            dn, dd = CASE_DTYPE[case]
+            extra[case] = _time_large_prefill(kda, inputs, 77, dev, seed, flush, barrier, agg_max, peak,
+                                              peak_kind, reps=3, lens=lens, H=H, name=name,
+                                              dtype_name=dn, d=dd)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -591,12 +599,21 @@ CASES = {
     # the 4096-token workload through kda_chunk_prefill_logdecay (g from the
     # bounded gate): the chunked path for an unbounded log-decay
     "prefill-unbounded": ("prefill-unbounded", 1, None),
+    # a 65,536-token sequence with 32 heads: the windowed split plan (as the
+    # 1M-token workload runs it) at a size an ncu capture can replay
+    "long-64k": ("long-64k: 1 seq x 65536 tokens", [65536], 32),
+    # the 4096-token layer in float32 and with 64-channel heads: the chunkwise
+    # float32 kernel on the CUDA cores
+    "prefill-f32": ("prefill-f32: 1 seq x 4096 tokens, float32", [4096], 16),
+    "prefill-d64": ("prefill-d64: 1 seq x 4096 tokens, dk=dv=64", [4096], 16),
 }
+CASE_DTYPE = {"prefill-f32": ("float32", 128), "prefill-d64": ("bfloat16", 64)}
 UNBOUNDED_CASES = {"prefill-unbounded"}
 
 
 def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, peak, peak_kind,
-                        reps=2, warm=1, lens=None, H=None, name=None, unbounded=False):
+                        reps=2, warm=1, lens=None, H=None, name=None, unbounded=False,
+                        dtype_name="bfloat16", d=128):
     """One KDA layer over a packed batch (by default the varlen or the 1M-token
     workload `wid`): inputs drawn on the device with the same distributions as
     the parity inputs (bf16 q/k L2-normalised, v/z N(0,1), beta = sigmoid(N(0,1)),
@@ -605,23 +622,24 @@ def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, pe
     if lens is None:
         w = inputs.workload(wid)
         lens, H, name = list(w.seq_lens), w.H, w.name
-    T, d = sum(lens), 128
+    T = sum(lens)
+    dt = getattr(torch, dtype_name)
     g = torch.Generator(device=dev)
     g.manual_seed(1000 + 7 * wid + seed)
 
     def normal(shape):
         return torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
 
-    q = torch.nn.functional.normalize(normal((T, H, d)), dim=-1).to(torch.bfloat16)
-    k = torch.nn.functional.normalize(normal((T, H, d)), dim=-1).to(torch.bfloat16)
-    v = normal((T, H, d)).to(torch.bfloat16)
-    z = normal((T, H, d)).to(torch.bfloat16)
+    q = torch.nn.functional.normalize(normal((T, H, d)), dim=-1).to(dt)
+    k = torch.nn.functional.normalize(normal((T, H, d)), dim=-1).to(dt)
+    v = normal((T, H, d)).to(dt)
+    z = normal((T, H, d)).to(dt)
     beta = torch.sigmoid(normal((T, H)))
     A = torch.rand((H, d), generator=g, device=dev) * 2 - 1
     cu = torch.zeros(len(lens) + 1, dtype=torch.int32, device=dev)
     cu[1:] = torch.cumsum(torch.tensor(lens, device=dev), 0)
     N = len(lens)
-    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, H, d), dtype=dt, device=dev)
     fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     if unbounded:   # the log-decay passed in (here the bounded gate's values)
@@ -649,12 +667,12 @@ def _time_large_prefill(kda, inputs, wid, dev, seed, flush, barrier, agg_max, pe
         barrier()
         times.append(e0.elapsed_time(e1) / 1000.0)
     t = agg_max(min(times))
-    alg = T * H * inputs.bytes_per_token_head(d, d, 2) + N * H * d * d * 4 + H * d * 4 + 4 * (N + 1)
+    alg = T * H * inputs.bytes_per_token_head(d, d, dt.itemsize) + N * H * d * d * 4 + H * d * 4 + 4 * (N + 1)
     ach = alg / t / 1e9
     status = kda.check_device_status(ws)
     del q, k, v, z, out, ws
     torch.cuda.empty_cache()
-    return {"workload": f"{name}: {N} seqs, {T} tokens, H={H}, dk=dv={d}, bf16, zero state",
+    return {"workload": f"{name}: {N} seqs, {T} tokens, H={H}, dk=dv={d}, {dtype_name}, zero state",
             "value": T / t, "unit": "tokens/s", "ms_per_call": 1000 * t,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                          "frac": ach / peak, "algorithmic_bytes_per_launch": alg,
@@ -694,6 +712,8 @@ def run_case(args):
     name, spec, H = CASES[args.case]
     peak, peak_kind = _peaks()
     kw = {} if isinstance(spec, int) else {"lens": spec, "H": H, "name": name}
+    if args.case in CASE_DTYPE:
+        kw["dtype_name"], kw["d"] = CASE_DTYPE[args.case]
     wid = spec if isinstance(spec, int) else 77
     r = _time_large_prefill(kda, inputs, wid, dev, 0, flush, torch.cuda.synchronize,
                             lambda x: x, peak, peak_kind, reps=args.steps, warm=args.warmup,
