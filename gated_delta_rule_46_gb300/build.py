@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkda_gb300.so")
 SOURCES = ["kda_api.cu", "kda_simt.cu", "kda_prefill_tc.cu", "kda_noalloc.cu", "kda_decode_pool.cu",
-           "kda_compose.cu", "kda_chunk_simt.cu"]
+           "kda_compose.cu", "kda_chunk_simt.cu", "kda_prefill_c32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "kda_common.cuh"
+#include "kda_tc_util.cuh"
 #include "kda_testing.h"
 #include "sm100_ptx.cuh"
 
@@ -128,66 +129,6 @@ __device__ __forceinline__ bool test_wait_expires(int mask, int bit, uint64_t *b
 // first row (and TMEM column) of right-factor tile a: 0, 16, 48, 96
 __device__ __forceinline__ int tile_off(int a) { return 8 * a * (a + 1); }
 
-// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` of a K-major,
-// 128B-swizzled operand (rows 128 B apart, chunk index XOR-ed with row % 8).
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float rcp(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-// 8 floats -> one 16-byte chunk of bf16.
-__device__ __forceinline__ void st_chunk(uint8_t *base, uint32_t off, const float *x) {
-    uint4 v;
-    v.x = pack_bf16(x[0], x[1]);
-    v.y = pack_bf16(x[2], x[3]);
-    v.z = pack_bf16(x[4], x[5]);
-    v.w = pack_bf16(x[6], x[7]);
-    *reinterpret_cast<uint4 *>(base + off) = v;
-}
-// one 16-byte chunk of bf16 -> 8 floats.
-__device__ __forceinline__ void ld_chunk(const uint8_t *base, uint32_t off, float *x) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(base + off);
-    const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(b[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
-}
-__device__ __forceinline__ void ld4(const float *p, float *x) {
-    const float4 v = *reinterpret_cast<const float4 *>(p);
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-}
-__device__ __forceinline__ void ld8(const float *p, float *x) { ld4(p, x); ld4(p + 4, x + 4); }
-
-// KSTEPS tcgen05 MMAs of K = 16 over K-major SW128 operands; K-blocks of 64
-// elements are a_kblk / b_kblk bytes apart.
-template <int KSTEPS>
-__device__ __forceinline__ void mma_k(uint32_t d, uint32_t a_addr, uint32_t a_kblk, uint32_t b_addr,
-                                      uint32_t b_kblk, uint32_t idesc, bool accumulate_first) {
-    const uint64_t a0 = ptx::sdesc_kmajor_sw128(a_addr), b0 = ptx::sdesc_kmajor_sw128(b_addr);
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-        const uint64_t a = a0 + (uint64_t)(((ks >> 2) * a_kblk + (ks & 3) * 32u) >> 4);
-        const uint64_t b = b0 + (uint64_t)(((ks >> 2) * b_kblk + (ks & 3) * 32u) >> 4);
-        ptx::mma_bf16_ss(d, a, b, idesc, (ks > 0 || accumulate_first) ? 1u : 0u);
-    }
-}
-
 // Per-thread view of the CTA: shared-memory pointers and the thread's roles.
 struct Ctx {
     uint8_t *sm;
@@ -214,10 +155,6 @@ __device__ __forceinline__ Ctx make_ctx(uint8_t *sm, uint32_t tmem) {
     x.ch = 32 * x.qw + x.lane;
     x.lane_base = tmem + ((uint32_t)(32 * x.qw) << 16);
     return x;
-}
-
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
 }
 
 // Phase A of a chunk: bounded gate, log2-domain cumulative decay and the
@@ -743,58 +680,6 @@ __device__ __forceinline__ void store_output(const Ctx &x, const CUtensorMap *tm
             }
         }
     }
-}
-
-// Sequence bounds with the kernel's own bounds check: malformed offsets are
-// reported and the sequence treated as empty.
-__device__ __forceinline__ void seq_bounds(const int32_t *cu, int seq, int64_t total, uint32_t *status,
-                                           int tid, int64_t &bos, int64_t &eos) {
-    bos = cu[seq];
-    eos = cu[seq + 1];
-    if (bos < 0 || eos < bos || eos > total) {
-        if (tid == 0) report_status(status, kDevBadSeqlens);
-        bos = eos = 0;
-    }
-}
-
-__device__ __forceinline__ void bulk_store(uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(gdst)),
-                 "r"(ptx::smem_addr(ssrc)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_copy_in(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
-                                             uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            ptx::smem_addr(sdst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar))
-        : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
-                                          uint64_t *bar) {
-    ptx::mbar_arrive_expect_tx(bar, bytes);
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            ptx::smem_addr(sdst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar))
-        : "memory");
-}
-
-// The same copies with an L2 cache policy.
-__device__ __forceinline__ void bulk_store_hint(uint8_t *gdst, const uint8_t *ssrc, uint32_t bytes, uint64_t pol) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
-                     reinterpret_cast<uint64_t>(gdst)),
-                 "r"(ptx::smem_addr(ssrc)), "r"(bytes), "l"(pol)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_copy_in_hint(uint8_t *sdst, const uint8_t *gsrc, uint32_t bytes,
-                                                  uint64_t *bar, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-            ptx::smem_addr(sdst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(ptx::smem_addr(bar)), "l"(pol)
-        : "memory");
 }
 
 // Slot of chunk c of sequence seq (first token bos), head h, in the diagonal-tile
@@ -2249,19 +2134,22 @@ static bool make_map_g(CUtensorMap *m, const float *base, int64_t T, int H) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [T, H*128] bf16 viewed as a 2-D tensor; 64 x 64 boxes, 128-byte swizzle,
-// rows beyond T read as zeros.
-static bool make_map(CUtensorMap *m, const void *base, int64_t T, int H) {
+// [T, H*128] bf16 viewed as a 2-D tensor; boxes of 64 channels x box_rows
+// tokens, 128-byte swizzle, rows beyond T read as zeros.
+bool make_map_bf16(CUtensorMap *m, const void *base, int64_t T, int H, int box_rows) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)H * 128, (cuuint64_t)T};
     cuuint64_t strides[1] = {(cuuint64_t)H * 128 * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+static bool make_map(CUtensorMap *m, const void *base, int64_t T, int H) {
+    return make_map_bf16(m, base, T, H, 64);
 }
 
 // Bytes of L2 on the current device.
@@ -2438,6 +2326,10 @@ static cudaError_t side_stream(SideStream **out) {
 
 cudaError_t launch_schedule(const int32_t *cu, int num_seqs, int32_t *order, uint32_t *counter,
                             uint32_t *status, cudaStream_t st);
+cudaError_t launch_prefill_c32(const void *q, const void *k, const void *v, const void *z, const float *A,
+                               const float *beta, const int32_t *cu, int num_seqs, int64_t total, int H,
+                               const float *s0, float *s1, void *out, int32_t *order, uint32_t *counter,
+                               uint32_t *status, int test_expire, int sms, cudaStream_t st);
 
 // Test support: the kExpire* bits the next tensor-core prefill call passes to
 // its kernels (kda_testing_expire_next_wait); taken, and cleared, by that call.
@@ -2776,6 +2668,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         return cudaGetLastError();
     }
 
+    return launch_prefill_c32(q, k, v, z, A, beta, cu, num_seqs, total, H, s0, s1, out, order, counter, status,
+                              test_expire, sms, st);
     e = cudaFuncSetAttribute(tc::prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)tc::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
