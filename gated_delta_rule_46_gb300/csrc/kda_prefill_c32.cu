@@ -160,12 +160,13 @@ __device__ __forceinline__ void save_state(const Ctx &x, float *dst) {
         for (int i = 0; i < 32; ++i) dst[(int64_t)(c0 + i) * D + x.ch] = X[i];
     }
 }
-// S^T <- S^T Diag(2^G_end) (the master only; the MMAs accumulate onto it)
-__device__ __forceinline__ void scale_state(const Ctx &x) {
+// S^T <- S^T Diag(2^G_end) on columns [c_lo, c_lo + 32 n) of this warp's lane
+// quarter (the master only; the MMAs accumulate onto it)
+__device__ __forceinline__ void scale_state(const Ctx &x, int c_lo, int n) {
 #pragma unroll 1
-    for (int m = 0; m < 2; ++m) {
+    for (int m = 0; m < n; ++m) {
         float X[32], g[32];
-        const int c0 = 64 * x.half + 32 * m;
+        const int c0 = c_lo + 32 * m;
         ptx::tmem_ld32(x.lane_base + TM_S + c0, X);
 #pragma unroll
         for (int i = 0; i < 32; i += 8) ld8(x.s_gamma + c0 + i, g + i);
@@ -245,10 +246,16 @@ __device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, uint64_t *bar_
         const float el0 = ok ? ex2(x0) : 0.f, el1 = ok ? ex2(x1) : 0.f;
         const float dd0 = ok ? ex2(-x0) : 0.f, dd1 = ok ? ex2(-x1) : 0.f;
         const float qe0 = qv.x * el0, qe1 = qv.y * el1, kh0 = kv.x * el0, kh1 = kv.y * el1;
-        *reinterpret_cast<uint32_t *>(qk + oq) = pack_bf16(qe0, qe1);          // Q^
-        *reinterpret_cast<uint32_t *>(qk + okk) = pack_bf16(kh0, kh1);         // K^
-        *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kh0 * rho0, kh1 * rho1);    // K~
-        *reinterpret_cast<uint32_t *>(b1 + okk) = pack_bf16(qe0 * rho0, qe1 * rho1);   // Q~
+        const uint32_t pq = pack_bf16(qe0, qe1), pk = pack_bf16(kh0, kh1);
+        *reinterpret_cast<uint32_t *>(qk + oq) = pq;                           // Q^
+        *reinterpret_cast<uint32_t *>(qk + okk) = pk;                          // K^
+        if (ta == 0) {   // R_0 = 0: K~ = K^ and Q~ = Q^
+            *reinterpret_cast<uint32_t *>(b1 + oq) = pk;
+            *reinterpret_cast<uint32_t *>(b1 + okk) = pq;
+        } else {
+            *reinterpret_cast<uint32_t *>(b1 + oq) = pack_bf16(kh0 * rho0, kh1 * rho1);    // K~
+            *reinterpret_cast<uint32_t *>(b1 + okk) = pack_bf16(qe0 * rho0, qe1 * rho1);   // Q~
+        }
         const float fr0 = kv.x * dd0, fr1 = kv.y * dd1;                        // k 2^(R_ta - G_t)
         kr0[i] = fr0 * ke0;
         kr1[i] = fr1 * ke1;
@@ -340,28 +347,44 @@ __device__ __forceinline__ void phase_diag(const Ctx &x) {
     for (int i = 0; i < 16; ++i) Ym[(b0 + i) * LS + b0 + x.lane] = y[i];
 }
 
-// The block below the diagonal, Y_10 = -D_1 L_10 D_0, as two float32 16 x 16
-// products (one output per thread), then T = Y Diag(beta) into its bf16 tile.
+// A barrier of warps 0 and 1 only (named barrier 1), so that the other warps
+// run on meanwhile.
+__device__ __forceinline__ void sync_w01() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+
+// Warps 0 and 1: the block below the diagonal, Y_10 = -D_1 L_10 D_0, as two
+// float32 16 x 16 products (four outputs per thread), then T = Y Diag(beta)
+// into its bf16 tile.
 __device__ __forceinline__ void phase_offdiag_T(const Ctx &x) {
     float *Lm = reinterpret_cast<float *>(x.sm + R_L);
     float *Ym = reinterpret_cast<float *>(x.sm + R_Y);
-    const int r = x.tid >> 4, cc = x.tid & 15;
+    const int u = x.tid;                       // 0 .. 63
+    const int r = u >> 2, c4 = 4 * (u & 3);    // row r, columns c4 .. c4 + 3
     {   // X = L_10 D_0 into the unused upper-right block of L
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc += Lm[(16 + r) * LS + m] * Ym[m * LS + cc];
-        Lm[r * LS + 16 + cc] = acc;
+        for (int m = 0; m < 16; ++m) {
+            const float l = Lm[(16 + r) * LS + m];
+            const float4 d = *reinterpret_cast<const float4 *>(Ym + m * LS + c4);
+            a0 += l * d.x; a1 += l * d.y; a2 += l * d.z; a3 += l * d.w;
+        }
+        *reinterpret_cast<float4 *>(Lm + r * LS + 16 + c4) = make_float4(a0, a1, a2, a3);
     }
-    __syncthreads();
+    sync_w01();
     {   // Y_10 = -D_1 X
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc += Ym[(16 + r) * LS + 16 + m] * Lm[m * LS + 16 + cc];
-        Ym[(16 + r) * LS + cc] = -acc;
+        for (int m = 0; m < 16; ++m) {
+            const float l = Ym[(16 + r) * LS + 16 + m];
+            const float4 d = *reinterpret_cast<const float4 *>(Lm + m * LS + 16 + c4);
+            a0 += l * d.x; a1 += l * d.y; a2 += l * d.z; a3 += l * d.w;
+        }
+        *reinterpret_cast<float4 *>(Ym + (16 + r) * LS + c4) = make_float4(-a0, -a1, -a2, -a3);
     }
-    __syncthreads();
-    if (x.tid < 128) {   // T [t][s] = Y [t][s] beta_s (s <= block of t), zero above: one 8-column chunk per thread
-        const int t = x.tid >> 2, p = x.tid & 3;
+    sync_w01();
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {   // T [t][s] = Y [t][s] beta_s (s <= block of t), zero above
+        const int e = u + 64 * rep;             // one 8-column chunk of a row
+        const int t = e >> 2, p = e & 3;
         const int a = t >> 4;
         float v[8], bt[8];
         ld8(Ym + t * LS + 8 * p, v);
@@ -564,10 +587,18 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (has_next) ++qk_issued;
             phase_extract(x);
             __syncthreads();
-            // ===== the inverse T = (I + L)^{-1} Diag(beta)
-            phase_diag(x);
-            __syncthreads();
-            phase_offdiag_T(x);
+            // ===== warps 0-1: the inverse T = (I + L)^{-1} Diag(beta); warps 2-7
+            // meanwhile: S^T <- S^T Diag(2^G_end) (warps 4 and 5 take the two lane
+            // quarters of warps 0 and 1 in full, warps 2, 3, 6, 7 half of theirs)
+            if (warp < 2) {
+                phase_diag(x);
+                sync_w01();
+                phase_offdiag_T(x);
+            } else if (warp == 4 || warp == 5) {
+                scale_state(x, 0, 4);
+            } else {
+                scale_state(x, 64 * x.half, 2);
+            }
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -583,7 +614,6 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 beta_next = 0.f;
                 if (next_row + tid < eos) beta_next = p.beta[(next_row + tid) * H + h];
             }
-            scale_state(x);    // the U MMA does not touch the master state
             if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
             phase_u_out(x);
