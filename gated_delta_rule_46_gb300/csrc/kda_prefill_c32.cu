@@ -351,36 +351,73 @@ __device__ __forceinline__ void phase_diag(const Ctx &x) {
 // run on meanwhile.
 __device__ __forceinline__ void sync_w01() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
-// Warps 0 and 1: the block below the diagonal, Y_10 = -D_1 L_10 D_0, as two
-// float32 16 x 16 products (four outputs per thread), then T = Y Diag(beta)
-// into its bf16 tile.
+// tf32 of a float32 (round to nearest, ties away)
+__device__ __forceinline__ uint32_t to_tf32(float f) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+    return r;
+}
+// d += a b for one m16n8k8 tile, tf32 inputs, float32 accumulation.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc (16 x 16, two n-tiles) = A (16 x 16 at Am, row stride LS) B (16 x 16 at
+// Bm), one warp; fragment layouts of m16n8k8 (g = lane / 4, q = lane % 4).
+__device__ __forceinline__ void warp_mm16(float (&acc)[2][4], const float *Am, const float *Bm, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        uint32_t a[4];
+        a[0] = to_tf32(Am[g * LS + 8 * ks + q]);
+        a[1] = to_tf32(Am[(g + 8) * LS + 8 * ks + q]);
+        a[2] = to_tf32(Am[g * LS + 8 * ks + q + 4]);
+        a[3] = to_tf32(Am[(g + 8) * LS + 8 * ks + q + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t b0 = to_tf32(Bm[(8 * ks + q) * LS + 8 * nt + g]);
+            const uint32_t b1 = to_tf32(Bm[(8 * ks + q + 4) * LS + 8 * nt + g]);
+            mma_tf32(acc[nt], a, b0, b1);
+        }
+    }
+}
+
+// Warps 0 and 1: the block below the diagonal, Y_10 = -D_1 L_10 D_0, on warp 0's
+// tf32 tensor-core MMAs (float32 accumulation; the diagonal blocks, solved
+// before in float32, carry the precision), then T = Y Diag(beta) into its bf16
+// tile by both warps.
 __device__ __forceinline__ void phase_offdiag_T(const Ctx &x) {
     float *Lm = reinterpret_cast<float *>(x.sm + R_L);
     float *Ym = reinterpret_cast<float *>(x.sm + R_Y);
+    if (x.warp == 0) {
+        const int g = x.lane >> 2, q = x.lane & 3;
+        float acc[2][4];
+        warp_mm16(acc, Lm + 16 * LS, Ym, x.lane);            // X = L_10 D_0
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {                      // X into the unused upper-right block of L
+            Lm[g * LS + 16 + 8 * nt + 2 * q] = acc[nt][0];
+            Lm[g * LS + 16 + 8 * nt + 2 * q + 1] = acc[nt][1];
+            Lm[(g + 8) * LS + 16 + 8 * nt + 2 * q] = acc[nt][2];
+            Lm[(g + 8) * LS + 16 + 8 * nt + 2 * q + 1] = acc[nt][3];
+        }
+        __syncwarp();
+        warp_mm16(acc, Ym + 16 * LS + 16, Lm + 16, x.lane);  // D_1 X
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {                      // Y_10 = -D_1 X
+            Ym[(16 + g) * LS + 8 * nt + 2 * q] = -acc[nt][0];
+            Ym[(16 + g) * LS + 8 * nt + 2 * q + 1] = -acc[nt][1];
+            Ym[(24 + g) * LS + 8 * nt + 2 * q] = -acc[nt][2];
+            Ym[(24 + g) * LS + 8 * nt + 2 * q + 1] = -acc[nt][3];
+        }
+    }
+    sync_w01();
     const int u = x.tid;                       // 0 .. 63
-    const int r = u >> 2, c4 = 4 * (u & 3);    // row r, columns c4 .. c4 + 3
-    {   // X = L_10 D_0 into the unused upper-right block of L
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float l = Lm[(16 + r) * LS + m];
-            const float4 d = *reinterpret_cast<const float4 *>(Ym + m * LS + c4);
-            a0 += l * d.x; a1 += l * d.y; a2 += l * d.z; a3 += l * d.w;
-        }
-        *reinterpret_cast<float4 *>(Lm + r * LS + 16 + c4) = make_float4(a0, a1, a2, a3);
-    }
-    sync_w01();
-    {   // Y_10 = -D_1 X
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float l = Ym[(16 + r) * LS + 16 + m];
-            const float4 d = *reinterpret_cast<const float4 *>(Lm + m * LS + 16 + c4);
-            a0 += l * d.x; a1 += l * d.y; a2 += l * d.z; a3 += l * d.w;
-        }
-        *reinterpret_cast<float4 *>(Ym + (16 + r) * LS + c4) = make_float4(-a0, -a1, -a2, -a3);
-    }
-    sync_w01();
 #pragma unroll
     for (int rep = 0; rep < 2; ++rep) {   // T [t][s] = Y [t][s] beta_s (s <= block of t), zero above
         const int e = u + 64 * rep;             // one 8-column chunk of a row
