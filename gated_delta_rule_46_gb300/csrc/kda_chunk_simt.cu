@@ -110,17 +110,17 @@ __global__ void __launch_bounds__(NT) prefill_chunk_simt_kernel(
                 G += sm.ke[t][c];
                 sm.ke[t][c] = G;
             }
-            const float Gend = G;
-            sm.gend[c] = expf(Gend);
+            const float gend = expf(G);
+            sm.gend[c] = gend;
 #pragma unroll
             for (int t = 0; t < C; ++t) {
                 const float Gt = sm.ke[t][c];
                 const float kk = sm.kh[t][c], qq = sm.qt[t][c];
-                const float eg = expf(Gt);
+                const float eg = expf(Gt), ieg = expf(-Gt);
                 sm.kt[t][c] = kk * eg;
                 sm.qt[t][c] = qq * eg;
-                sm.kh[t][c] = kk * expf(-Gt);
-                sm.ke[t][c] = kk * expf(Gend - Gt);
+                sm.kh[t][c] = kk * ieg;
+                sm.ke[t][c] = (kk * ieg) * gend;   // k e^{G_end - G_t}
             }
         }
         __syncthreads();
