@@ -25,7 +25,7 @@
 // Per chunk: A gate, decay, operands (SIMT) | MMA Gram/P (N = 48) and
 // [K~S | Q~S] (N = 64) | RHS^T = V^T - (K~S)^T | P, L out of TMEM | the inverse:
 // two diagonal 16 x 16 blocks by float32 forward substitution and the block
-// below them as two float32 16 x 16 products | U^T = RHS^T T^T (MMA, while the
+// below them as two 16 x 16 products on warp-level tf32 MMAs | U^T = RHS^T T^T (MMA, while the
 // master state is scaled by e^{G_end}) | O^T += U^T P^T, S^T += U^T Kend (MMA) |
 // the bf16 state copy and the output tile (TMA store).
 #include <cuda.h>
