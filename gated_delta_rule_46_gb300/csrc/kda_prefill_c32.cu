@@ -518,7 +518,8 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint64_t *bar_v = bar_qk + 2;
     uint64_t *bar_g = bar_qk + 3;      // Gram/P MMA done
     uint64_t *bar_s = bar_qk + 4;      // state MMA done
-    uint64_t *bar_m = bar_qk + 5;      // U MMA, then output/state MMAs done
+    uint64_t *bar_m = bar_qk + 5;      // U MMA, then the output MMA done
+    uint64_t *bar_m2 = bar_qk + 6;     // the state update MMA done (thread 32)
     uint64_t *bar_never = bar_qk + 7;  // test support: nothing arrives here
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + R_SLOT);
     volatile int *s_work = reinterpret_cast<volatile int *>(sm + R_SLOT + 4);
@@ -551,6 +552,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
     uint32_t g_issued = 0, g_done = 0, s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
+    uint32_t m2_issued = 0, m2_done = 0;
     const int n_work = p.num_seqs * H;
     bool first = true;
 
@@ -596,6 +598,8 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             ptx::tc_fence_before_sync();
             __syncthreads();
             if (*s_abort) break;
+            // One thread issues a tcgen05.mma only about every 100 cycles, so the
+            // two independent products go to two issuing threads.
             if (tid == 0) {
                 ptx::tc_fence_after_sync();
                 if (has_next) tma_2box(sm + R_Z, &tm_z, hx, (int)next_row, bar_z);   // z is read
@@ -603,6 +607,8 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 mma_k<8>(tmem + TM_G, sbase + R_QK, 8192u, sbase + R_GB, GB_KB, ptx::idesc_bf16_f32(128, 48),
                          false);
                 ptx::mma_commit(bar_g);
+            } else if (tid == 32) {
+                ptx::tc_fence_after_sync();
                 // state product: D1[j][s | t] = S^T[j] . [K~; Q~][s | t]
                 mma_k<8>(tmem + TM_D1, sbase + R_ST, 16384u, sbase + R_B1, 8192u, ptx::idesc_bf16_f32(128, 64),
                          false);
@@ -660,13 +666,19 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (*s_abort) break;
             if (tid == 0) {
                 ptx::tc_fence_after_sync();
-                // O^T += U^T P^T (onto the Q~S0 half of D1);  S^T += U^T Kend
+                // O^T += U^T P^T (onto the Q~S0 half of D1)
                 mma_k<2>(tmem + TM_D1 + 32, sbase + R_RU, 0u, sbase + R_P, 0u, ptx::idesc_bf16_f32(128, 32), true);
-                mma_k<2>(tmem + TM_S, sbase + R_RU, 0u, sbase + R_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
                 ptx::mma_commit(bar_m);
+            } else if (tid == 32) {
+                ptx::tc_fence_after_sync();
+                // S^T += U^T Kend
+                mma_k<2>(tmem + TM_S, sbase + R_RU, 0u, sbase + R_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
+                ptx::mma_commit(bar_m2);
             }
             ++m_issued;
+            ++m2_issued;
             if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
+            if (ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
             if (tid == 0 && has_next) tma_2box(sm + R_V, &tm_v, hx, (int)next_row, bar_v);   // P, T are read
             if (has_next) ++v_issued;
@@ -692,6 +704,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         while (g_done < g_issued && ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done;
         while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
         while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
+        while (m2_done < m2_issued && ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done;
     }
     if (tid == 0) ptx::bulk_wait_all();
     ptx::tc_fence_before_sync();

@@ -1222,7 +1222,8 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint64_t *bar_qk = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *bar_z = bar_qk + 1;
     uint64_t *bar_v = bar_qk + 2;
-    uint64_t *bar_g = bar_qk + 3;      // Gram/P MMA, then W/U~ MMAs done
+    uint64_t *bar_g = bar_qk + 3;      // Gram/P MMA, then the W MMA done
+    uint64_t *bar_g2 = bar_qk + 5;     // the U~ MMA done (issued by thread 32)
     uint64_t *bar_d = bar_qk + 4;      // UNB: the item's diagonal tiles staged
     uint64_t *bar_never = bar_qk + 7;  // test support: nothing arrives here
     // UNB: the diagonal tiles are staged behind P (free until U~^T is staged)
@@ -1257,7 +1258,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const Ctx x = make_ctx(sm, tmem);
 
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
-    uint32_t g_issued = 0, g_done = 0, d_issued = 0, d_done = 0;
+    uint32_t g_issued = 0, g_done = 0, d_issued = 0, d_done = 0, g2_issued = 0, g2_done = 0;
     // inputs are read once (evict first); the records are read back by the next
     // kernels of the call (evict last), and the last reader discards them
     // (only when the records of the call fit in L2; plain copies otherwise)
@@ -1393,19 +1394,27 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ptx::tc_fence_before_sync();
         __syncthreads();
         if (*s_abort) break;
+        // the two products from two issuing threads (one thread issues a
+        // tcgen05.mma only about every 100 cycles)
         if (tid == 0) {
             ptx::tc_fence_after_sync();
             ptx::bulk_wait_read();   // P has left its tile (U~^T staging goes there)
             // W[t][c] = T[t] . K~^T[c] (rows t >= 64 of the left operand run over
-            // the next tile and are discarded) and U~^T[j][t] = V^T[j] . T[t]
+            // the next tile and are discarded)
             mma_k<4>(tmem + TM_W, sbase + OFF_TB_INTRA, 0u, sbase + OFF_KT, 0u,
                      ptx::idesc_bf16_f32(128, 128), false);
+            ptx::mma_commit(bar_g);
+        } else if (tid == 32) {
+            ptx::tc_fence_after_sync();
+            // U~^T[j][t] = V^T[j] . T[t]
             mma_k<4>(tmem + TM_UT, sbase + OFF_VT, 0u, sbase + OFF_TB_INTRA, 0u,
                      ptx::idesc_bf16_f32(128, 64), false);
-            ptx::mma_commit(bar_g);
+            ptx::mma_commit(bar_g2);
         }
         ++g_issued;
+        ++g2_issued;
         if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
+        if (ptx::mbar_wait(bar_g2, g2_done & 1, kWaitBudget)) ++g2_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
         phase_wu_out(x);
         ptx::fence_async_smem();
@@ -1429,6 +1438,7 @@ prefill_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         while (z_done < z_issued && ptx::mbar_wait(bar_z, z_done & 1, kWaitBudget)) ++z_done;
         while (v_done < v_issued && ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done;
         while (g_done < g_issued && ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done;
+        while (g2_done < g2_issued && ptx::mbar_wait(bar_g2, g2_done & 1, kWaitBudget)) ++g2_done;
         while (d_done < d_issued && ptx::mbar_wait(bar_d, d_done & 1, kWaitBudget)) ++d_done;
     }
     if (tid == 0) ptx::bulk_wait_all();
@@ -1754,8 +1764,12 @@ prefill_seg_kernel(const SplitParams p) {
                                               ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(sm);
     uint64_t *bar_st = reinterpret_cast<uint64_t *>(sm + SG_BAR);   // [2] stages
-    uint64_t *bar_s = bar_st + 2;
-    uint64_t *bar_m = bar_st + 3;
+    // the S0 chain's products are issued by thread 0, the M chain's by thread
+    // 32 (two issuing threads keep the tensor core about twice as busy)
+    uint64_t *bar_s = bar_st + 2;      // U products (thread 0: S0)
+    uint64_t *bar_m = bar_st + 3;      // state products (thread 0: S0)
+    uint64_t *bar_s2 = bar_st + 4;     // U product (thread 32: M)
+    uint64_t *bar_m2 = bar_st + 5;     // state product (thread 32: M)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SG_BAR + 64);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + SG_BAR + 72);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1793,6 +1807,7 @@ prefill_seg_kernel(const SplitParams p) {
 
     uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
     uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
+    uint32_t s2_done = 0, m2_done = 0;   // (issued with s, m)
     if (tid == 0) {
         for (int k = 0; k < 2; ++k)
             if (c0 + k < c_end) load_stage_seg(sm + k * SG_STAGE, recs + (size_t)(c0 + k) * REC_BYTES, bar_st + k, p.rec_in_l2);
@@ -1815,12 +1830,16 @@ prefill_seg_kernel(const SplitParams p) {
         const uint32_t sstg = sbase + k * SG_STAGE;
         if (tid == 0) {
             ptx::tc_fence_after_sync();
-            // U^T = U~^T + S0^T (-W)^T ;  U_M^T = M^T (-W)^T
+            // U^T = U~^T + S0^T (-W)^T
             mma_k<8>(tmem + TG_U, sbase + SG_ST, 16384u, sstg + SG_NW, 8192u,
                      ptx::idesc_bf16_f32(128, 64), true);
+            ptx::mma_commit(bar_s);
+        } else if (tid == 32) {
+            ptx::tc_fence_after_sync();
+            // U_M^T = M^T (-W)^T
             mma_k<8>(tmem + TG_UM, sbase + SG_MT, 16384u, sstg + SG_NW, 8192u,
                      ptx::idesc_bf16_f32(128, 64), false);
-            ptx::mma_commit(bar_s);
+            ptx::mma_commit(bar_s2);
         }
         ++s_issued;
         // the two master states are not touched by those MMAs: scale them meanwhile
@@ -1828,6 +1847,7 @@ prefill_seg_kernel(const SplitParams p) {
         scale_state(x, TG_S, gamma);
         scale_state(x, TG_M, gamma);
         if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
+        if (ptx::mbar_wait(bar_s2, s2_done & 1, kWaitBudget)) ++s2_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
         u_out(x, TG_U, SG_RU);
         u_out(x, TG_UM, SG_RUM);
@@ -1837,10 +1857,14 @@ prefill_seg_kernel(const SplitParams p) {
         if (*s_abort) break;
         if (tid == 0) {
             ptx::tc_fence_after_sync();
-            // S0^T += U^T Kend ;  M^T += U_M^T Kend
+            // S0^T += U^T Kend
             mma_k<4>(tmem + TG_S, sbase + SG_RU, 0u, sstg + SG_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
-            mma_k<4>(tmem + TG_M, sbase + SG_RUM, 0u, sstg + SG_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
             ptx::mma_commit(bar_m);
+        } else if (tid == 32) {
+            ptx::tc_fence_after_sync();
+            // M^T += U_M^T Kend
+            mma_k<4>(tmem + TG_M, sbase + SG_RUM, 0u, sstg + SG_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
+            ptx::mma_commit(bar_m2);
         }
         ++m_issued;
         if (c + 1 < c_end) {   // meanwhile: the next chunk's U~^T
@@ -1849,6 +1873,7 @@ prefill_seg_kernel(const SplitParams p) {
             preload_u64(x, TG_U, sm + (k ^ 1) * SG_STAGE + SG_UT);
         }
         if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
+        if (ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
         state_to_bf16(x, TG_S, SG_ST);
         state_to_bf16(x, TG_M, SG_MT);
@@ -1877,7 +1902,9 @@ prefill_seg_kernel(const SplitParams p) {
         for (int k = 0; k < 2; ++k)
             while (st_done[k] < st_issued[k] && ptx::mbar_wait(bar_st + k, st_done[k] & 1, kWaitBudget)) ++st_done[k];
         while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
+        while (s2_done < s_issued && ptx::mbar_wait(bar_s2, s2_done & 1, kWaitBudget)) ++s2_done;
         while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
+        while (m2_done < m_issued && ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done;
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
