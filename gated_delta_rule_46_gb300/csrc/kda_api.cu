@@ -49,11 +49,16 @@ cudaError_t launch_decode_tokens(const void *q, const void *k, const void *v, co
                                  const float *A, const float *beta, float *pool, int pool_size,
                                  const int32_t *slots, void *out, int N, int n_tok, int H, int dk,
                                  int dv, bool bf16, uint32_t *status, cudaStream_t st);
+cudaError_t launch_decode_tokens_tc(const void *q, const void *k, const void *v, const void *z, const float *A,
+                                    const float *beta, float *pool, int pool_size, const int32_t *slots, void *out,
+                                    int N, int n_tokens, int H, uint32_t *status, int sms, cudaStream_t st);
 }  // namespace kda
 
 namespace {
 
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+// from this many tokens per sequence kda_decode_tokens runs the chunked form
+constexpr int kDecodeTcMinTokens = 4;
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
 
@@ -227,6 +232,19 @@ kda_status_t kda_decode_tokens(const void *q, const void *k, const void *v, cons
     if (!slot_ids && pool_size < N) return KDA_ERR_INVALID_ARG;
     if (!q || !k || !v || !z || !A || !beta || !state_pool || !out) return KDA_ERR_INVALID_ARG;
     if (!aligned(state_pool, 16)) return KDA_ERR_INVALID_ARG;
+    // Several tokens per sequence, bf16, 128 x 128 heads: the chunked form on the
+    // tensor cores (the tokens of a sequence as chunks of the fused prefill
+    // kernel, the state from and back to its slot); one or a few tokens: the
+    // token-serial kernel, which moves only the state.
+    if (dtype == KDA_BF16 && dk == 128 && dv == 128 && n_tokens >= kDecodeTcMinTokens && aligned(q, 16) &&
+        aligned(k, 16) && aligned(v, 16) && aligned(z, 16) && aligned(out, 16)) {
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        return from_cuda(kda::launch_decode_tokens_tc(q, k, v, z, A, beta, state_pool, pool_size, slot_ids, out,
+                                                      N, n_tokens, H, status, sms,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(kda::launch_decode_tokens(q, k, v, z, A, beta, state_pool, pool_size, slot_ids,
                                                out, N, n_tokens, H, dk, dv, dtype == KDA_BF16,
                                                status, reinterpret_cast<cudaStream_t>(stream)));

@@ -106,6 +106,15 @@ struct Params {
     int num_seqs;
     int H;
     int test_expire;
+    // state-pool mode (kda_decode_tokens) when pool != nullptr: sequence i is
+    // tokens [i L, (i + 1) L), L = uniform_len, and its state is pool slot
+    // slots[i] (or i), read and written in place; a negative slot is a padding
+    // row (zero outputs, no state), a slot >= pool_size is reported and padded.
+    // Chains are taken in order, CTA b the chains b, b + grid, ...
+    float *pool;
+    const int32_t *slots;
+    int pool_size;
+    int uniform_len;
 };
 
 struct Ctx {
@@ -193,8 +202,15 @@ __device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, uint64_t *bar_
     const uint32_t cb = (uint32_t)(lane >> 2), co = (uint32_t)(lane & 3) * 4u;
     const float2 ea = *reinterpret_cast<const float2 *>(x.s_eAn + c);
     if (ptx::mbar_wait(bar_z, z_done & 1, kWaitBudget)) ++z_done; else *s_abort = 1;
+    // a group of rows wholly past the chunk's valid rows (a short decode chunk,
+    // a ragged tail) only writes zero operand rows (warp-uniform)
+    const bool empty = 8 * h >= nvalid;
     float g0[8], g1[8];
-    {
+    if (empty) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g0[i] = g1[i] = 0.f;
+        *reinterpret_cast<float2 *>(x.s_ht + h * 128 + c) = make_float2(0.f, 0.f);
+    } else {
         const uint8_t *zt = sm + R_Z + kb * 4096;
         float run0 = 0.f, run1 = 0.f;
 #pragma unroll
@@ -235,6 +251,23 @@ __device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, uint64_t *bar_
     uint8_t *b1 = sm + R_B1 + kb * 8192;
     uint8_t *gb = sm + R_GB + kb * GB_KB;
     float kr0[8], kr1[8];
+    if (empty) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * h + i;
+            const uint32_t oq = swz(t, cb) + co, okk = swz(32 + t, cb) + co;
+            *reinterpret_cast<uint32_t *>(qk + oq) = 0u;
+            *reinterpret_cast<uint32_t *>(qk + okk) = 0u;
+            *reinterpret_cast<uint32_t *>(b1 + oq) = 0u;
+            *reinterpret_cast<uint32_t *>(b1 + okk) = 0u;
+            *reinterpret_cast<uint32_t *>(gb + swz(toff(ta) + t, cb) + co) = 0u;
+            if (ta == 0) *reinterpret_cast<uint32_t *>(gb + swz(toff(1) + t, cb) + co) = 0u;
+            kr0[i] = kr1[i] = 0.f;
+        }
+        st_chunk(sm + R_KE, swz(c, h), kr0);
+        st_chunk(sm + R_KE, swz(c + 1, h), kr1);
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int t = 8 * h + i;
@@ -556,18 +589,44 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int n_work = p.num_seqs * H;
     bool first = true;
 
+    const bool pool_mode = p.pool != nullptr;
+    int next_static = blockIdx.x;
     for (;;) {
-        if (tid == 0) *s_work = (int)atomicAdd(p.counter, 1u);
+        if (pool_mode) {
+            if (tid == 0) *s_work = next_static;
+            next_static += gridDim.x;
+        } else if (tid == 0) {
+            *s_work = (int)atomicAdd(p.counter, 1u);
+        }
         __syncthreads();
         const int w = *s_work;
         if (w >= n_work || *s_abort) break;
-        const int seq = p.order[w / H];
+        const int seq = pool_mode ? w / H : p.order[w / H];
         const int h = w % H;
-        int64_t bos, eos;
-        seq_bounds(p.cu_seqlens, seq, p.total_tokens, p.status, tid, bos, eos);
-        const int nchunks = (int)((eos - bos + C - 1) / C);
-        const int64_t sidx = ((int64_t)seq * H + h) * D * D;
         const int hx = h * D;
+        int64_t bos, eos;
+        const float *s_init;
+        float *s_fin;
+        if (pool_mode) {
+            bos = (int64_t)seq * p.uniform_len;
+            eos = bos + p.uniform_len;
+            const int slot = p.slots ? p.slots[seq] : seq;
+            if (slot < 0 || slot >= p.pool_size) {   // padding row: zero outputs, no state
+                if (slot >= p.pool_size && tid == 0) report_status(p.status, kDevBadSeqlens);
+                for (int e = tid; e < p.uniform_len * 16; e += NT)
+                    *reinterpret_cast<uint4 *>(p.out + (bos + e / 16) * rowstride + hx + (e % 16) * 8) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                __syncthreads();   // (*s_work is rewritten by the next item)
+                continue;
+            }
+            s_init = s_fin = p.pool + ((size_t)slot * H + h) * D * D;
+        } else {
+            seq_bounds(p.cu_seqlens, seq, p.total_tokens, p.status, tid, bos, eos);
+            const int64_t sidx = ((int64_t)seq * H + h) * D * D;
+            s_init = p.initial_state ? p.initial_state + sidx : nullptr;
+            s_fin = p.final_state ? p.final_state + sidx : nullptr;
+        }
+        const int nchunks = (int)((eos - bos + C - 1) / C);
 
         if (nchunks > 0 && tid == 0) {
             tma_qk(sm, &tm_q, &tm_k, hx, (int)bos, bar_qk);
@@ -575,7 +634,17 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tma_2box(sm + R_V, &tm_v, hx, (int)bos, bar_v);
         }
         if (nchunks > 0) { ++qk_issued; ++z_issued; ++v_issued; }
-        load_state(x, p.initial_state ? p.initial_state + sidx : nullptr);
+        load_state(x, s_init);
+        if (pool_mode) {   // the next chain's state into L2 while this one runs (64 KB, 512 lines)
+            const int wn = w + (int)gridDim.x;
+            if (wn < n_work) {
+                const int sn = p.slots ? p.slots[wn / H] : wn / H;
+                if (sn >= 0 && sn < p.pool_size) {
+                    const uint8_t *nx = reinterpret_cast<const uint8_t *>(p.pool + ((size_t)sn * H + wn % H) * D * D);
+                    for (int i = tid; i < D * D * 4 / 128; i += NT) ptx::prefetch_l2(nx + (size_t)i * 128);
+                }
+            }
+        }
         if (tid < D) x.s_eAn[tid] = -expf(p.A[h * D + tid]) * kLog2e;
         float beta_next = 0.f;
         if (tid < C && bos + tid < eos) beta_next = p.beta[(bos + tid) * H + h];
@@ -690,7 +759,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             store_output(x, &tm_o, p.out, row0, nvalid, hx, rowstride);
         }
         if (*s_abort) break;
-        if (p.final_state) save_state(x, p.final_state + sidx);
+        if (s_fin) save_state(x, s_fin);
         ptx::tc_fence_before_sync();
         __syncthreads();
     }
@@ -745,6 +814,7 @@ cudaError_t launch_prefill_c32(const void *q, const void *k, const void *v, cons
     prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order; prm.counter = counter;
     prm.status = status; prm.total_tokens = total; prm.num_seqs = num_seqs; prm.H = H;
     prm.test_expire = test_expire;
+    prm.pool = nullptr; prm.slots = nullptr; prm.pool_size = 0; prm.uniform_len = 0;
     const int64_t chains = (int64_t)num_seqs * H;
     const int64_t cap = 2 * (int64_t)sms;
     const unsigned grid = (unsigned)(chains < cap ? chains : cap);
@@ -759,6 +829,33 @@ cudaError_t launch_prefill_c32(const void *q, const void *k, const void *v, cons
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, c32::prefill_c32_kernel, mq, mk, mv, mz, mo, prm);
+}
+
+// kda_decode_tokens on the tensor cores (bf16, dk = dv = 128): the n tokens of
+// every sequence are one or more chunks of the one-kernel prefill, its state
+// read from and written back to its pool slot.
+cudaError_t launch_decode_tokens_tc(const void *q, const void *k, const void *v, const void *z, const float *A,
+                                    const float *beta, float *pool, int pool_size, const int32_t *slots, void *out,
+                                    int N, int n_tokens, int H, uint32_t *status, int sms, cudaStream_t st) {
+    const int64_t total = (int64_t)N * n_tokens;
+    CUtensorMap mq, mk, mv, mz, mo;
+    if (!make_map_bf16(&mq, q, total, H, c32::C) || !make_map_bf16(&mk, k, total, H, c32::C) ||
+        !make_map_bf16(&mv, v, total, H, c32::C) || !make_map_bf16(&mz, z, total, H, c32::C) ||
+        !make_map_bf16(&mo, out, total, H, c32::C))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(c32::prefill_c32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)c32::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    c32::Params prm{};
+    prm.A = A; prm.beta = beta; prm.cu_seqlens = nullptr; prm.initial_state = nullptr; prm.final_state = nullptr;
+    prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = nullptr; prm.counter = nullptr;
+    prm.status = status; prm.total_tokens = total; prm.num_seqs = N; prm.H = H; prm.test_expire = 0;
+    prm.pool = pool; prm.slots = slots; prm.pool_size = pool_size; prm.uniform_len = n_tokens;
+    const int64_t chains = (int64_t)N * H;
+    const int64_t cap = 2 * (int64_t)sms;
+    const unsigned grid = (unsigned)(chains < cap ? chains : cap);
+    c32::prefill_c32_kernel<<<grid, c32::NT, c32::SMEM_ALLOC, st>>>(mq, mk, mv, mz, mo, prm);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -123,6 +123,10 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
 }
 // Drops the 128-byte L2 line at `p` (128-byte aligned) without writing it back:
 // for scratch data that no one reads again.  Its contents become undefined.
+// Fetches the 128-byte line holding p into L2 (no registers written).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ void discard_l2(const void *p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
 }

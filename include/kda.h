@@ -255,6 +255,11 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
  *   status      device uint32, or NULL; e.g. the first word of a prefill
  *               workspace, then read with kda_check_device_status()
  * Supported: dk, dv in {32, 64, 128}, any n_tokens >= 0.
+ * With bf16 inputs, dk = dv = 128, n_tokens >= 4 and 16-byte aligned q, k, v,
+ * z, out, the tokens of a sequence are processed in the chunked form on the
+ * tensor cores (as kda_chunk_prefill does: results agree with the token-serial
+ * form to bf16 rounding, not bit for bit); otherwise token by token in
+ * float32.
  */
 kda_status_t kda_decode_tokens(const void *q, const void *k, const void *v, const void *z,
                                const float *A, const float *beta, float *state_pool,

@@ -81,6 +81,35 @@ def test_bad_slot_is_recorded_and_skipped():
     assert not torch.equal(pool[0], torch.ones_like(pool[0]))
 
 
+def test_tensor_core_path_two_chunks_and_bad_slot():
+    """bf16 128 x 128 heads with several tokens per sequence run the chunked
+    form on the tensor cores: 40 tokens (a full and a ragged 32-token chunk)
+    per sequence against the oracle, a padding row and a bad slot (recorded,
+    padded, no state touched)."""
+    dev = need_gpu()
+    N, n, H, P = 5, 40, 2, 6
+    slots = [4, 9, 0, -1, 2]
+    b = _batch(N, n, H, 128, 128, torch.bfloat16, wid=45)
+    rng = np.random.default_rng(45)
+    pool = torch.from_numpy((0.1 * rng.standard_normal((P, H, 128, 128))).astype(np.float32))
+    pool_dev = pool.to(dev)
+    status = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = decode_tokens(*(b[x].to(dev) for x in ("q", "k", "v", "z", "A", "beta")), pool_dev,
+                        slot_ids=torch.tensor(slots, dtype=torch.int32, device=dev), status=status)
+    assert kda.check_device_status(status) == kda.KDA_ERR_INVALID_ARG
+    init = np.stack([pool[s].double().numpy() if 0 <= s < P else np.zeros((H, 128, 128)) for s in slots])
+    f = b["flat"]
+    ro, rf = oracle.prefill(f["q"], f["k"], f["v"], f["z"], f["A"], f["beta"], f["cu_seqlens"], init)
+    ro = ro.reshape(N, n, H, 128)
+    live = [0, 2, 4]
+    assert_close("outputs", out[live], ro[live], torch.bfloat16)
+    assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[3]) == 0
+    got = pool_dev.cpu()
+    assert_close("states", got[[slots[i] for i in live]], rf[live], torch.bfloat16)
+    for s_ in (1, 3, 5):
+        assert torch.equal(got[s_], pool[s_]), s_
+
+
 def test_invalid_arguments():
     dev = need_gpu()
     b = _batch(2, 1, 1, 32, 32, torch.float32, wid=44)
