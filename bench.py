@@ -428,6 +428,8 @@ def run_gpu(args):
     # (token-serial kernel), g taken from the bounded gate so both compute one layer
     ablation = _time_unbounded_gate(kda, g1, fin1, out1, ws1, flush, barrier, agg_max, stream,
                                     T1, tp / K)
+    # ---- the same prefill without a workspace (kda_chunk_prefill_noalloc)
+    noalloc = _time_noalloc(kda, g1, fin1, out1, flush, barrier, agg_max, stream, T1, tp / K)
 
     # ---- the two large prefill workloads, inputs generated on the device
     extra = {}
@@ -482,6 +484,7 @@ def run_gpu(args):
             "decode_tokens": multi,
             "prefill_large": extra,
             "prefill_unbounded_gate": ablation,
+            "prefill_noalloc": noalloc,
             "gpu_launches": K * (L_pref + NS),   # the timed step; decode_tokens and prefill_large are timed apart
             "clocks": clk.result,
             "device_status": ok_status,
@@ -586,6 +589,33 @@ def _time_unbounded_gate(kda, g1, fin1, out1, ws1, flush, barrier, agg_max, stre
             "us_per_call": t * 1e6, "value": T1 / t, "unit": "tokens/s",
             "token_serial_us_per_call": t_serial * 1e6,
             "bounded_chunked_us_per_call": t_bounded * 1e6}
+
+
+def _time_noalloc(kda, g1, fin1, out1, flush, barrier, agg_max, stream, T1, t_plan, reps=5):
+    """The 4096-token prefill through kda_chunk_prefill_noalloc: no caller
+    workspace, so always the one-kernel plan (here 16 chains on 16 CTA
+    slots), against the segment-scan plan that the workspace allows."""
+    import torch
+
+    def call():
+        kda.chunk_prefill_noalloc(g1["q"], g1["k"], g1["v"], g1["z"], g1["A"], g1["beta"], g1["cu_seqlens"],
+                                  g1["initial_state"], final_state=fin1, out=out1)
+    call()
+    barrier()
+    times = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        barrier()
+        times.append(e0.elapsed_time(e1) / 1000.0)
+    t = agg_max(min(times))
+    return {"workload": f"the same prefill (T={T1}) through kda_chunk_prefill_noalloc: no workspace, "
+                        "so the one-kernel plan (one CTA per chain); the L2 flushed before each call",
+            "us_per_call": t * 1e6, "value": T1 / t, "unit": "tokens/s",
+            "segment_scan_us_per_call": t_plan * 1e6}
 
 
 # Prefill cases timed on their own (`--case`), e.g. as the command an ncu

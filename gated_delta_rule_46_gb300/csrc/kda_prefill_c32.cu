@@ -74,8 +74,8 @@ constexpr uint32_t R_BETA = 110592;    // 32 float
 constexpr uint32_t R_EAN = R_BETA + 128;     // 128 float: -exp(A) log2(e)
 constexpr uint32_t R_HT = R_EAN + 512;       // [4][128] float: sums of the log2 decay per 8-token group
 constexpr uint32_t R_GAMMA = R_HT + 2048;    // 128 float: 2^(G_end)
-constexpr uint32_t R_BAR = R_GAMMA + 512;    // 8 mbarriers
-constexpr uint32_t R_SLOT = R_BAR + 64;      // TMEM base, work item, abort flag
+constexpr uint32_t R_BAR = R_GAMMA + 512;    // 16 mbarriers
+constexpr uint32_t R_SLOT = R_BAR + 128;     // TMEM base, work item, abort flag
 constexpr uint32_t SMEM_USED = R_SLOT + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // slack to align the base to 1024 B
 static_assert(R_GB + 2 * GB_KB <= R_Z && R_Y + C * LS * 4 <= R_Z && R_OST + 8192 <= R_Z, "R_GB region");
@@ -144,6 +144,27 @@ __device__ __forceinline__ Ctx make_ctx(uint8_t *sm, uint32_t tmem) {
 // ---- state --------------------------------------------------------------------
 // Master S^T [j][c] into TMEM and its bf16 copy into the state operand tile; this
 // thread holds c in [64 half, 64 half + 64) of row j.  src == nullptr: zeros.
+// The same from the float32 state [c][j] that a chain start bulk-copied into
+// shared memory (rows 0-63 over the [K~; Q~] and Kend regions, rows 64-127
+// over the state operand tile): every thread reads its 64 values first, then
+// the bf16 copy overwrites the second half (a block barrier between).
+__device__ __forceinline__ void load_state_staged(const Ctx &x) {
+    const float *rows = reinterpret_cast<const float *>(x.sm + (x.half ? R_ST : R_B1));
+    float Sm[2][32];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) Sm[m][i] = rows[(32 * m + i) * D + x.ch];
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+            st_chunk(x.sm + R_ST + x.half * 16384, swz(x.ch, 4 * m + q4), &Sm[m][8 * q4]);
+        ptx::tmem_st32(x.lane_base + TM_S + 64 * x.half + 32 * m, Sm[m]);
+    }
+    ptx::tmem_st_wait();
+}
 __device__ __forceinline__ void load_state(const Ctx &x, const float *src) {
 #pragma unroll 1
     for (int m = 0; m < 2; ++m) {
@@ -554,6 +575,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint64_t *bar_m = bar_qk + 5;      // U MMA, then the output MMA done
     uint64_t *bar_m2 = bar_qk + 6;     // the state update MMA done (thread 32)
     uint64_t *bar_never = bar_qk + 7;  // test support: nothing arrives here
+    uint64_t *bar_st = bar_qk + 8;     // a chain's start state bulk-copied into shared memory
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + R_SLOT);
     volatile int *s_work = reinterpret_cast<volatile int *>(sm + R_SLOT + 4);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + R_SLOT + 8);
@@ -562,7 +584,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int64_t rowstride = (int64_t)H * D;
 
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) ptx::mbar_init(bar_qk + i, 1);
+        for (int i = 0; i < 9; ++i) ptx::mbar_init(bar_qk + i, 1);
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
@@ -585,7 +607,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     uint32_t qk_issued = 0, qk_done = 0, z_issued = 0, z_done = 0, v_issued = 0, v_done = 0;
     uint32_t g_issued = 0, g_done = 0, s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
-    uint32_t m2_issued = 0, m2_done = 0;
+    uint32_t m2_issued = 0, m2_done = 0, st_issued = 0, st_done = 0;
     const int n_work = p.num_seqs * H;
     bool first = true;
 
@@ -628,13 +650,30 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         const int nchunks = (int)((eos - bos + C - 1) / C);
 
-        if (nchunks > 0 && tid == 0) {
-            tma_qk(sm, &tm_q, &tm_k, hx, (int)bos, bar_qk);
-            tma_2box(sm + R_Z, &tm_z, hx, (int)bos, bar_z);
-            tma_2box(sm + R_V, &tm_v, hx, (int)bos, bar_v);
+        // the start state by two bulk copies (the copy engine keeps all 64 KB in
+        // flight; per-thread loads of the columns would wait several memory round
+        // trips), when it is 16-byte aligned
+        const bool staged = s_init && (reinterpret_cast<uintptr_t>(s_init) & 15) == 0;
+        if (tid == 0) {
+            if (staged) {
+                ptx::mbar_arrive_expect_tx(bar_st, 65536);
+                bulk_copy_in(sm + R_B1, reinterpret_cast<const uint8_t *>(s_init), 32768, bar_st);
+                bulk_copy_in(sm + R_ST, reinterpret_cast<const uint8_t *>(s_init + 64 * D), 32768, bar_st);
+            }
+            if (nchunks > 0) {
+                tma_qk(sm, &tm_q, &tm_k, hx, (int)bos, bar_qk);
+                tma_2box(sm + R_Z, &tm_z, hx, (int)bos, bar_z);
+                tma_2box(sm + R_V, &tm_v, hx, (int)bos, bar_v);
+            }
         }
         if (nchunks > 0) { ++qk_issued; ++z_issued; ++v_issued; }
-        load_state(x, s_init);
+        if (staged) {
+            ++st_issued;
+            if (ptx::mbar_wait(bar_st, st_done & 1, kWaitBudget)) ++st_done; else *s_abort = 1;
+            load_state_staged(x);
+        } else {
+            load_state(x, s_init);
+        }
         if (pool_mode) {   // the next chain's state into L2 while this one runs (64 KB, 512 lines)
             const int wn = w + (int)gridDim.x;
             if (wn < n_work) {
@@ -774,6 +813,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
         while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
         while (m2_done < m2_issued && ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done;
+        while (st_done < st_issued && ptx::mbar_wait(bar_st, st_done & 1, kWaitBudget)) ++st_done;
     }
     if (tid == 0) ptx::bulk_wait_all();
     ptx::tc_fence_before_sync();
