@@ -313,7 +313,7 @@ __device__ __forceinline__ void phase_gate_operands(const Ctx &x, int nvalid, ui
 __device__ __forceinline__ void phase_extract_PL(const Ctx &x, uint32_t off_pb,
                                                  const float *diag = nullptr) {
     uint8_t *sm = x.sm;
-    const int warp = x.warp, lane = x.lane, qw = x.qw, cg = x.cg;
+    const int lane = x.lane, qw = x.qw, cg = x.cg;
     const uint32_t lane_base = x.lane_base;
     float *s_beta = x.s_beta;
     float *Lm = x.Lm;
@@ -2697,18 +2697,6 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
 
     return launch_prefill_c32(q, k, v, z, A, beta, cu, num_seqs, total, H, s0, s1, out, order, counter, status,
                               test_expire, sms, st);
-    e = cudaFuncSetAttribute(tc::prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tc::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    const int grid = (int)(chains < sms ? chains : sms);
-    tc::Params prm;
-    prm.A = A; prm.beta = beta; prm.cu_seqlens = cu; prm.initial_state = s0;
-    prm.final_state = s1; prm.out = static_cast<__nv_bfloat16 *>(out); prm.order = order;
-    prm.counter = counter; prm.status = status; prm.total_tokens = total;
-    prm.num_seqs = num_seqs; prm.H = H; prm.diag = nullptr; prm.diag_stride = 0;
-    prm.test_expire = test_expire;
-    return launch_pdl(tc::prefill_tc_kernel<false>, (unsigned)grid, tc::NT, tc::SMEM_ALLOC, st, mq, mk, mv, mz,
-                      mo, prm);
 }
 
 }  // namespace kda
