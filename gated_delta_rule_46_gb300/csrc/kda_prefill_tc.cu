@@ -1491,7 +1491,9 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     const uint32_t sbase = ptx::smem_addr(sm);
     uint64_t *bar_st = reinterpret_cast<uint64_t *>(sm + SB_BAR);   // [2] record stages
     uint64_t *bar_s = bar_st + 2;
-    uint64_t *bar_m = bar_st + 3;
+    uint64_t *bar_m = bar_st + 3;      // the state update (thread 0)
+    uint64_t *bar_m2 = bar_st + 4;     // the output product (thread 32: one thread issues a
+                                       // tcgen05.mma only about every 100 cycles)
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SB_BAR + 64);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + SB_BAR + 72);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1565,7 +1567,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     };
 
     uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
-    uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0;
+    uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0, m2_done = 0;
     const int c0 = w0;
     if (tid == 0) {
         for (int k = 0; k < 2; ++k)
@@ -1613,10 +1615,14 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         if (*s_abort) break;
         if (tid == 0) {
             ptx::tc_fence_after_sync();
-            // O^T += U^T P^T ; S^T += U^T Kend
-            mma_k<4>(tmem + d1 + 64, sbase + SB_RU, 0u, sstg + REC_PB, 0u, ptx::idesc_bf16_f32(128, 64), true);
+            // S^T += U^T Kend
             mma_k<4>(tmem + TS_D3, sbase + SB_RU, 0u, sstg + REC_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
             ptx::mma_commit(bar_m);
+        } else if (tid == 32) {
+            ptx::tc_fence_after_sync();
+            // O^T += U^T P^T
+            mma_k<4>(tmem + d1 + 64, sbase + SB_RU, 0u, sstg + REC_PB, 0u, ptx::idesc_bf16_f32(128, 64), true);
+            ptx::mma_commit(bar_m2);
         }
         ++m_issued;
         // meanwhile: the next chunk's [U~ | 0] into the other D1 buffer
@@ -1630,6 +1636,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
             preload_u(x, TS_D1 + 128 * (k ^ 1), sm + (k ^ 1) * SB_STAGE + REC_UT);
         }
         if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
+        if (ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
         phase_state_out(x, TS_D3, d1 + 64, SB_ST, SB_RU);
         ptx::fence_async_smem();
@@ -1655,6 +1662,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
             while (st_done[k] < st_issued[k] && ptx::mbar_wait(bar_st + k, st_done[k] & 1, kWaitBudget)) ++st_done[k];
         while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
         while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
+        while (m2_done < m_issued && ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done;
     }
     if (tid == 0) ptx::bulk_wait_all();
     ptx::tc_fence_before_sync();
