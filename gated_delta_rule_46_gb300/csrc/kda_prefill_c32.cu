@@ -378,8 +378,8 @@ __device__ __forceinline__ void phase_extract(const Ctx &x) {
 
 // Warps 0 and 1 (lanes 0-15): the diagonal blocks D_a = (I + L_aa)^{-1} by
 // forward substitution in float32, one column per lane, into Y.
-__device__ __forceinline__ void phase_diag(const Ctx &x) {
-    if (x.warp >= 2 || x.lane >= 16) return;
+__device__ __forceinline__ void phase_diag(const Ctx &x, int nblocks = 2) {
+    if (x.warp >= nblocks || x.lane >= 16) return;
     const float *Lm = reinterpret_cast<const float *>(x.sm + R_L);
     float *Ym = reinterpret_cast<float *>(x.sm + R_Y);
     const int b0 = 16 * x.warp;
@@ -482,6 +482,32 @@ __device__ __forceinline__ void phase_offdiag_T(const Ctx &x) {
         ld8(x.s_beta + 8 * p, bt);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = (8 * p + i < 16 * (a + 1)) ? v[i] * bt[i] : 0.f;
+        st_chunk(x.sm + R_T, swz(t, p), v);
+    }
+}
+
+// A chunk with at most 16 valid rows: its second tile is empty (zero L rows,
+// zero beta), so T = D_0 Diag(beta) in the first 16 x 16 block and zero
+// elsewhere.  Warps 0 and 1, after warp 0 has solved D_0 (phase_diag with one
+// block).
+__device__ __forceinline__ void phase_T_single(const Ctx &x) {
+    const float *Ym = reinterpret_cast<const float *>(x.sm + R_Y);
+    const int u = x.tid;                       // 0 .. 63
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+        const int e = u + 64 * rep;             // one 8-column chunk of a row
+        const int t = e >> 2, p = e & 3;
+        float v[8];
+        if (t < 16 && p < 2) {
+            float bt[8];
+            ld8(Ym + t * LS + 8 * p, v);
+            ld8(x.s_beta + 8 * p, bt);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] *= bt[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        }
         st_chunk(x.sm + R_T, swz(t, p), v);
     }
 }
@@ -742,9 +768,15 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // meanwhile: S^T <- S^T Diag(2^G_end) (warps 4 and 5 take the two lane
             // quarters of warps 0 and 1 in full, warps 2, 3, 6, 7 half of theirs)
             if (warp < 2) {
-                phase_diag(x);
-                sync_w01();
-                phase_offdiag_T(x);
+                if (nvalid <= 16) {   // one 16-token tile (a short decode chunk, a ragged tail)
+                    phase_diag(x, 1);
+                    sync_w01();
+                    phase_T_single(x);
+                } else {
+                    phase_diag(x);
+                    sync_w01();
+                    phase_offdiag_T(x);
+                }
             } else if (warp == 4 || warp == 5) {
                 scale_state(x, 0, 4);
             } else {
@@ -757,7 +789,11 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (tid == 0) {
                 ptx::tc_fence_after_sync();
                 // U^T = RHS^T T^T
-                mma_k<2>(tmem + TM_U, sbase + R_RU, 0u, sbase + R_T, 0u, ptx::idesc_bf16_f32(128, 32), false);
+                // (at most 16 valid rows: the tokens past 16 contribute zeros, one K step)
+                if (nvalid <= 16)
+                    mma_k<1>(tmem + TM_U, sbase + R_RU, 0u, sbase + R_T, 0u, ptx::idesc_bf16_f32(128, 32), false);
+                else
+                    mma_k<2>(tmem + TM_U, sbase + R_RU, 0u, sbase + R_T, 0u, ptx::idesc_bf16_f32(128, 32), false);
                 ptx::mma_commit(bar_m);
             }
             ++m_issued;
@@ -775,12 +811,18 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (tid == 0) {
                 ptx::tc_fence_after_sync();
                 // O^T += U^T P^T (onto the Q~S0 half of D1)
-                mma_k<2>(tmem + TM_D1 + 32, sbase + R_RU, 0u, sbase + R_P, 0u, ptx::idesc_bf16_f32(128, 32), true);
+                if (nvalid <= 16)
+                    mma_k<1>(tmem + TM_D1 + 32, sbase + R_RU, 0u, sbase + R_P, 0u, ptx::idesc_bf16_f32(128, 32), true);
+                else
+                    mma_k<2>(tmem + TM_D1 + 32, sbase + R_RU, 0u, sbase + R_P, 0u, ptx::idesc_bf16_f32(128, 32), true);
                 ptx::mma_commit(bar_m);
             } else if (tid == 32) {
                 ptx::tc_fence_after_sync();
                 // S^T += U^T Kend
-                mma_k<2>(tmem + TM_S, sbase + R_RU, 0u, sbase + R_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
+                if (nvalid <= 16)
+                    mma_k<1>(tmem + TM_S, sbase + R_RU, 0u, sbase + R_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
+                else
+                    mma_k<2>(tmem + TM_S, sbase + R_RU, 0u, sbase + R_KE, 0u, ptx::idesc_bf16_f32(128, 128), true);
                 ptx::mma_commit(bar_m2);
             }
             ++m_issued;
