@@ -546,6 +546,22 @@ __device__ __forceinline__ void phase_state_out(const Ctx &x) {
         *reinterpret_cast<__nv_bfloat16 *>(x.sm + obox + swz(t, jc) + jo) = __float2bfloat16_rn(O[i]);
     }
 }
+// Only O^T into the output tile (the last chunk of a chain in state-pool
+// mode: nobody reads the bf16 state copy, its region receives the next
+// chain's start state).
+__device__ __forceinline__ void phase_o_out(const Ctx &x) {
+    float O[16];
+    ptx::tmem_ld16(x.lane_base + TM_D1 + 32 + 16 * x.half, O);
+    ptx::tmem_ld_wait();
+    const int j = x.ch;
+    const uint32_t obox = R_OST + (uint32_t)(j >> 6) * 4096u;
+    const uint32_t jc = (uint32_t)((j & 63) >> 3), jo = (uint32_t)(j & 7) * 2u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int t = 16 * x.half + i;
+        *reinterpret_cast<__nv_bfloat16 *>(x.sm + obox + swz(t, jc) + jo) = __float2bfloat16_rn(O[i]);
+    }
+}
 
 // The staged output tile to global memory (after a block barrier): one TMA
 // store per 64-channel box for a full chunk, 16-byte stores of the rows <
@@ -585,6 +601,9 @@ __device__ __forceinline__ void tma_qk(uint8_t *sm, const CUtensorMap *tq, const
     ptx::tma_load_2d(sm + R_QK + 12288, tk, hx + 64, y, bar);
 }
 
+// POOL: the state-pool mode (kda_decode_tokens); the prefill instantiation
+// carries none of its code.
+template <bool POOL>
 __global__ void __launch_bounds__(NT, 2)
 prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_z,
@@ -637,8 +656,9 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int n_work = p.num_seqs * H;
     bool first = true;
 
-    const bool pool_mode = p.pool != nullptr;
+    constexpr bool pool_mode = POOL;
     int next_static = blockIdx.x;
+    const float *pre_init = nullptr;   // a start state whose bulk copy the previous chain issued
     for (;;) {
         if (pool_mode) {
             if (tid == 0) *s_work = next_static;
@@ -680,8 +700,10 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // flight; per-thread loads of the columns would wait several memory round
         // trips), when it is 16-byte aligned
         const bool staged = s_init && (reinterpret_cast<uintptr_t>(s_init) & 15) == 0;
+        const bool pre = staged && s_init == pre_init;   // already in flight
+        pre_init = nullptr;
         if (tid == 0) {
-            if (staged) {
+            if (staged && !pre) {
                 ptx::mbar_arrive_expect_tx(bar_st, 65536);
                 bulk_copy_in(sm + R_B1, reinterpret_cast<const uint8_t *>(s_init), 32768, bar_st);
                 bulk_copy_in(sm + R_ST, reinterpret_cast<const uint8_t *>(s_init + 64 * D), 32768, bar_st);
@@ -694,7 +716,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         if (nchunks > 0) { ++qk_issued; ++z_issued; ++v_issued; }
         if (staged) {
-            ++st_issued;
+            if (!pre) ++st_issued;
             if (ptx::mbar_wait(bar_st, st_done & 1, kWaitBudget)) ++st_done; else *s_abort = 1;
             load_state_staged(x);
         } else {
@@ -755,7 +777,9 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (ptx::mbar_wait(bar_v, v_done & 1, kWaitBudget)) ++v_done; else *s_abort = 1;
             if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            phase_rhs(x, nvalid);
+            // (a state-pool chunk of at most 16 valid rows: the U product takes one K
+            // step, token columns 0-15, so the warps of columns 16-31 skip)
+            if (!(pool_mode && nvalid <= 16 && x.half)) phase_rhs(x, nvalid);
             // ===== P and L out of TMEM (P goes over v, read above)
             if (ptx::mbar_wait(bar_g, g_done & 1, kWaitBudget)) ++g_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
@@ -803,7 +827,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
             if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
             ptx::tc_fence_after_sync();
-            phase_u_out(x);
+            if (!(pool_mode && nvalid <= 16 && x.half)) phase_u_out(x);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -832,7 +856,27 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             ptx::tc_fence_after_sync();
             if (tid == 0 && has_next) tma_2box(sm + R_V, &tm_v, hx, (int)next_row, bar_v);   // P, T are read
             if (has_next) ++v_issued;
-            phase_state_out(x);
+            if (pool_mode && !has_next) {
+                // the chain's last products are done, so its staging regions are free:
+                // the next chain's start state starts arriving now, during the output
+                // and the state save, instead of at the next chain's start
+                const int wn = w + (int)gridDim.x;
+                if (wn < n_work) {
+                    const int sn = p.slots ? p.slots[wn / H] : wn / H;
+                    if (sn >= 0 && sn < p.pool_size) {
+                        pre_init = p.pool + ((size_t)sn * H + wn % H) * D * D;
+                        if (tid == 0) {
+                            ptx::mbar_arrive_expect_tx(bar_st, 65536);
+                            bulk_copy_in(sm + R_B1, reinterpret_cast<const uint8_t *>(pre_init), 32768, bar_st);
+                            bulk_copy_in(sm + R_ST, reinterpret_cast<const uint8_t *>(pre_init + 64 * D), 32768,
+                                         bar_st);
+                        }
+                        ++st_issued;
+                    }
+                }
+            }
+            if (pre_init) phase_o_out(x);
+            else phase_state_out(x);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
@@ -888,7 +932,7 @@ cudaError_t launch_prefill_c32(const void *q, const void *k, const void *v, cons
         !make_map_bf16(&mv, v, total, H, c32::C) || !make_map_bf16(&mz, z, total, H, c32::C) ||
         !make_map_bf16(&mo, out, total, H, c32::C))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(c32::prefill_c32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(c32::prefill_c32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)c32::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     c32::Params prm;
@@ -910,7 +954,7 @@ cudaError_t launch_prefill_c32(const void *q, const void *k, const void *v, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, c32::prefill_c32_kernel, mq, mk, mv, mz, mo, prm);
+    return cudaLaunchKernelEx(&cfg, c32::prefill_c32_kernel<false>, mq, mk, mv, mz, mo, prm);
 }
 
 // kda_decode_tokens on the tensor cores (bf16, dk = dv = 128): the n tokens of
@@ -925,7 +969,7 @@ cudaError_t launch_decode_tokens_tc(const void *q, const void *k, const void *v,
         !make_map_bf16(&mv, v, total, H, c32::C) || !make_map_bf16(&mz, z, total, H, c32::C) ||
         !make_map_bf16(&mo, out, total, H, c32::C))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(c32::prefill_c32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(c32::prefill_c32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)c32::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     c32::Params prm{};
@@ -936,7 +980,7 @@ cudaError_t launch_decode_tokens_tc(const void *q, const void *k, const void *v,
     const int64_t chains = (int64_t)N * H;
     const int64_t cap = 2 * (int64_t)sms;
     const unsigned grid = (unsigned)(chains < cap ? chains : cap);
-    c32::prefill_c32_kernel<<<grid, c32::NT, c32::SMEM_ALLOC, st>>>(mq, mk, mv, mz, mo, prm);
+    c32::prefill_c32_kernel<true><<<grid, c32::NT, c32::SMEM_ALLOC, st>>>(mq, mk, mv, mz, mo, prm);
     return cudaGetLastError();
 }
 
