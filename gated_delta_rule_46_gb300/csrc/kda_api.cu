@@ -237,7 +237,7 @@ kda_status_t kda_decode_tokens(const void *q, const void *k, const void *v, cons
     // kernel, the state from and back to its slot); one or a few tokens: the
     // token-serial kernel, which moves only the state.
     if (dtype == KDA_BF16 && dk == 128 && dv == 128 && n_tokens >= kDecodeTcMinTokens && aligned(q, 16) &&
-        aligned(k, 16) && aligned(v, 16) && aligned(z, 16) && aligned(out, 16)) {
+        aligned(k, 16) && aligned(v, 16) && aligned(z, 16) && aligned(out, 16) && aligned(state_pool, 16)) {
         int dev = 0, sms = 148;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -256,7 +256,7 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
  *               workspace, then read with kda_check_device_status()
  * Supported: dk, dv in {32, 64, 128}, any n_tokens >= 0.
  * With bf16 inputs, dk = dv = 128, n_tokens >= 4 and 16-byte aligned q, k, v,
- * z, out, the tokens of a sequence are processed in the chunked form on the
+ * z, out and state_pool, the tokens of a sequence are processed in the chunked form on the
  * tensor cores (as kda_chunk_prefill does: results agree with the token-serial
  * form to bf16 rounding, not bit for bit); otherwise token by token in
  * float32.

@@ -110,6 +110,41 @@ def test_tensor_core_path_two_chunks_and_bad_slot():
         assert torch.equal(got[s_], pool[s_]), s_
 
 
+@pytest.mark.parametrize("n", [8, 40])
+def test_tensor_core_path_many_chains_per_cta(n):
+    """768 (sequence, head) chains, more than the persistent grid's 2 x SMs
+    CTAs, so every CTA runs several chains in a row and fetches the next
+    chain's start state and inputs during its current chain's last chunk.
+    Padding rows and a bad slot sit where some chains' successors land.
+    Outputs and states against the oracle."""
+    dev = need_gpu()
+    N, H, P = 96, 8, 112
+    rng = np.random.default_rng(46 + n)
+    slots = [int(s) for s in rng.permutation(P)[:N]]
+    for i in (10, 50, 95):
+        slots[i] = -1
+    slots[61] = P + 5
+    b = _batch(N, n, H, 128, 128, torch.bfloat16, wid=46 + n)
+    pool = torch.from_numpy((0.1 * rng.standard_normal((P, H, 128, 128))).astype(np.float32))
+    pool_dev = pool.to(dev)
+    status = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = decode_tokens(*(b[x].to(dev) for x in ("q", "k", "v", "z", "A", "beta")), pool_dev,
+                        slot_ids=torch.tensor(slots, dtype=torch.int32, device=dev), status=status)
+    assert kda.check_device_status(status) == kda.KDA_ERR_INVALID_ARG
+    init = np.stack([pool[s].double().numpy() if 0 <= s < P else np.zeros((H, 128, 128)) for s in slots])
+    f = b["flat"]
+    ro, rf = oracle.prefill(f["q"], f["k"], f["v"], f["z"], f["A"], f["beta"], f["cu_seqlens"], init)
+    ro = ro.reshape(N, n, H, 128)
+    live = [i for i, s in enumerate(slots) if 0 <= s < P]
+    assert_close("outputs", out[live], ro[live], torch.bfloat16)
+    for i in (10, 50, 61, 95):
+        assert torch.count_nonzero(out[i]) == 0, i
+    got = pool_dev.cpu()
+    assert_close("states", got[[slots[i] for i in live]], rf[live], torch.bfloat16)
+    for s_ in sorted(set(range(P)) - {slots[i] for i in live}):
+        assert torch.equal(got[s_], pool[s_]), s_
+
+
 def test_invalid_arguments():
     dev = need_gpu()
     b = _batch(2, 1, 1, 32, 32, torch.float32, wid=44)
