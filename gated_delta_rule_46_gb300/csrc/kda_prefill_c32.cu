@@ -786,7 +786,9 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             __syncthreads();
             if (tid == 0 && has_next) tma_qk(sm, &tm_q, &tm_k, hx, (int)next_row, bar_qk);   // [Q^;K^] read
             if (has_next) ++qk_issued;
-            phase_extract(x);
+            // (columns s >= 16 of P and L feed neither the one-tile inverse nor the
+            // one-K-step output product)
+            if (!(pool_mode && nvalid <= 16 && x.half)) phase_extract(x);
             __syncthreads();
             // ===== warps 0-1: the inverse T = (I + L)^{-1} Diag(beta); warps 2-7
             // meanwhile: S^T <- S^T Diag(2^G_end) (warps 4 and 5 take the two lane
@@ -875,8 +877,11 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                 }
             }
-            if (pre_init) phase_o_out(x);
-            else phase_state_out(x);
+            if (pre_init) {
+                if (!(nvalid <= 16 && x.half)) phase_o_out(x);   // rows >= 16 are not stored
+            } else {
+                phase_state_out(x);
+            }
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
