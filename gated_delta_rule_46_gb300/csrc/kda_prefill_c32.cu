@@ -213,9 +213,13 @@ __device__ __forceinline__ void scale_state(const Ctx &x, int c_lo, int n) {
 // eight rows 8h .. 8h + 7, h = w & 3 (16-token tile h / 2).  The chunk-local log2
 // decay is summed in registers; the four group sums per channel are exchanged
 // through shared memory.  Writes [Q^; K^] in place, [K~; Q~], the right factors
-// of the two Gram/P row tiles, Kend^T and 2^(G_end).
-__device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, uint64_t *bar_z, uint32_t &z_done,
-                                        uint64_t *bar_qk, uint32_t &qk_done, volatile int *s_abort) {
+// of the two Gram/P row tiles, Kend^T and 2^(G_end).  one_tile (at most 16 valid
+// rows, every later product restricted to rows and columns 0-15): the rows of
+// tile 1 and the tile-1 right factors are left as they are, as nothing reads
+// what they feed.
+__device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, bool one_tile, uint64_t *bar_z,
+                                        uint32_t &z_done, uint64_t *bar_qk, uint32_t &qk_done,
+                                        volatile int *s_abort) {
     uint8_t *sm = x.sm;
     const int lane = x.lane, h = x.warp & 3, kb = x.warp >> 2;
     const int ta = h >> 1;
@@ -268,6 +272,7 @@ __device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, uint64_t *bar_
     const float ke0 = ex2(R20 - Rt0), ke1 = ex2(R21 - Rt1);         // 2^(G_end - R_ta)
     const float f0 = ex2(R10), f1 = ex2(R11);                       // 2^(R_1 - R_0) (tile 0 rows only)
     if (ptx::mbar_wait(bar_qk, qk_done & 1, kWaitBudget)) ++qk_done; else *s_abort = 1;
+    if (one_tile && ta == 1) return;
     uint8_t *qk = sm + R_QK + kb * 8192;
     uint8_t *b1 = sm + R_B1 + kb * 8192;
     uint8_t *gb = sm + R_GB + kb * GB_KB;
@@ -282,7 +287,7 @@ __device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, uint64_t *bar_
             *reinterpret_cast<uint32_t *>(b1 + oq) = 0u;
             *reinterpret_cast<uint32_t *>(b1 + okk) = 0u;
             *reinterpret_cast<uint32_t *>(gb + swz(toff(ta) + t, cb) + co) = 0u;
-            if (ta == 0) *reinterpret_cast<uint32_t *>(gb + swz(toff(1) + t, cb) + co) = 0u;
+            if (ta == 0 && !one_tile) *reinterpret_cast<uint32_t *>(gb + swz(toff(1) + t, cb) + co) = 0u;
             kr0[i] = kr1[i] = 0.f;
         }
         st_chunk(sm + R_KE, swz(c, h), kr0);
@@ -314,7 +319,7 @@ __device__ __forceinline__ void phase_a(const Ctx &x, int nvalid, uint64_t *bar_
         kr0[i] = fr0 * ke0;
         kr1[i] = fr1 * ke1;
         *reinterpret_cast<uint32_t *>(gb + swz(toff(ta) + t, cb) + co) = pack_bf16(fr0, fr1);
-        if (ta == 0)   // tile 0 tokens also appear in tile 1's block: k 2^(R_1 - G_t)
+        if (ta == 0 && !one_tile)   // tile 0 tokens also appear in tile 1's block: k 2^(R_1 - G_t)
             *reinterpret_cast<uint32_t *>(gb + swz(toff(1) + t, cb) + co) = pack_bf16(fr0 * f0, fr1 * f1);
     }
     st_chunk(sm + R_KE, swz(c, h), kr0);
@@ -749,7 +754,7 @@ prefill_c32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 !ptx::mbar_wait(bar_never, 0, kTestWaitBudget))
                 *s_abort = 1;
             first = false;
-            phase_a(x, nvalid, bar_z, z_done, bar_qk, qk_done, s_abort);
+            phase_a(x, nvalid, pool_mode && nvalid <= 16, bar_z, z_done, bar_qk, qk_done, s_abort);
             ptx::fence_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
