@@ -110,14 +110,15 @@ def test_tensor_core_path_two_chunks_and_bad_slot():
         assert torch.equal(got[s_], pool[s_]), s_
 
 
-@pytest.mark.parametrize("n", [8, 13, 40, 45])
+@pytest.mark.parametrize("n", [4, 8, 13, 32, 33, 40, 45])
 def test_tensor_core_path_many_chains_per_cta(n):
     """768 (sequence, head) chains, more than the persistent grid's 2 x SMs
     CTAs, so every CTA runs several chains in a row and fetches the next
     chain's start state and inputs during its current chain's last chunk.
     Padding rows and a bad slot sit where some chains' successors land.
-    Last chunks of 8 and 13 valid rows (one 16-token tile, one or two 8-row
-    groups). Outputs and states against the oracle."""
+    Last chunks of 4, 8 and 13 valid rows (one 16-token tile, one or two 8-row
+    groups), a full 32-row chunk and a 1-row tail. Outputs and states against
+    the oracle."""
     dev = need_gpu()
     N, H, P = 96, 8, 112
     rng = np.random.default_rng(46 + n)
