@@ -56,6 +56,21 @@ def _src_sha(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def _packed_layout(tensors):
+    """Byte offsets of named tensors packed into one buffer (256-byte aligned
+    pieces): (layout, total bytes, views(buf) -> the tensors as views of buf).
+    One pinned buffer per step then crosses to the device in one copy."""
+    layout, nbytes = {}, 0
+    for n, t in tensors.items():
+        size = t.numel() * t.element_size()
+        layout[n] = (nbytes, t.dtype, tuple(t.shape), size)
+        nbytes += (size + 255) // 256 * 256
+
+    def views(buf):
+        return {n: buf[o:o + sz].view(dt).view(shp) for n, (o, dt, shp, sz) in layout.items()}
+    return layout, nbytes, views
+
+
 def _ncu_traffic(kernel_key, src_file):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel source has changed since the counters were taken."""
@@ -291,20 +306,17 @@ def run_gpu(args):
     # inputs travel while step i - 1 computes and step i - 1's outputs travel
     # back.  e2e = work / wall time of the whole pipelined run (first copy in to
     # last copy out), so a copy that does not overlap counts in full.
-    pin = {n: t.pin_memory() for n, t in d1.items() if isinstance(t, torch.Tensor)}
+    # the prefill's inputs in one pinned buffer (one copy per step), device
+    # buffers of the same layout
+    pref_t = {n: t for n, t in d1.items() if isinstance(t, torch.Tensor)}
+    _, pref_bytes, pref_views = _packed_layout(pref_t)
+    pin = torch.empty(pref_bytes, dtype=torch.uint8).pin_memory()
+    for n, v in pref_views(pin).items():
+        v.copy_(pref_t[n])
     host_out1 = [torch.empty((T1, H1, 128), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     host_fin1 = [torch.empty((1, H1, 128, 128), dtype=torch.float32).pin_memory() for _ in range(2)]
-    # each decode step's inputs (q, k, v, z, beta) in one pinned buffer, 256-byte
-    # aligned pieces, so that a step is one host-to-device copy; the device
-    # buffers hold views of the same layout
-    layout, step_bytes = {}, 0
-    for n, t in host_steps[0].items():
-        layout[n] = (step_bytes, t.dtype, tuple(t.shape), t.numel() * t.element_size())
-        step_bytes += (t.numel() * t.element_size() + 255) // 256 * 256
-
-    def step_views(buf):
-        return {n: buf[o:o + nb].view(dt).view(shp) for n, (o, dt, shp, nb) in layout.items()}
-
+    # each decode step's inputs (q, k, v, z, beta) likewise
+    _, step_bytes, step_views = _packed_layout(host_steps[0])
     pin_steps = []
     for hs in host_steps:
         buf = torch.empty(step_bytes, dtype=torch.uint8).pin_memory()
@@ -313,12 +325,13 @@ def run_gpu(args):
         pin_steps.append(buf)
     host_out4 = [torch.empty((w4.decode_N, w4.H, 128), dtype=torch.bfloat16).pin_memory()
                  for _ in range(NS)]
-    h2d_pref = sum(t.numel() * t.element_size() for t in pin.values())
+    h2d_pref = pref_bytes
     d2h_pref = host_out1[0].numel() * 2 + host_fin1[0].numel() * 4
     h2d_dec = NS * step_bytes
     d2h_dec = NS * host_out4[0].numel() * 2
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    gb = [{n: torch.empty_like(t) for n, t in g1.items() if isinstance(t, torch.Tensor)} for _ in range(2)]
+    gbuf = [torch.empty(pref_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    gb = [pref_views(buf) for buf in gbuf]
     ob = [torch.empty_like(out1) for _ in range(2)]
     fb = [torch.empty_like(fin1) for _ in range(2)]
     dbuf = [torch.empty(step_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
@@ -362,8 +375,7 @@ def run_gpu(args):
         return e0.elapsed_time(e1) / 1000.0
 
     def pref_in(i, b):
-        for n, t in pin.items():
-            gb[b][n].copy_(t, non_blocking=True)
+        gbuf[b].copy_(pin, non_blocking=True)
 
     def pref_compute(i, b):
         flush.fill_(float(i))
