@@ -616,16 +616,19 @@ __device__ __forceinline__ void phase_rhs(const Ctx &x, uint32_t tm_ks, uint32_t
 // S^T <- S^T Diag(2^G_end) in TMEM (the dS MMA then accumulates onto it).  It
 // touches only the master state, so it can run while an MMA that does not
 // write the master (the U product) is in flight.
-__device__ __forceinline__ void scale_state(const Ctx &x, uint32_t tm_s, const float *gamma) {
+__device__ __forceinline__ void scale_state_cols(const Ctx &x, uint32_t tm_s, const float *gamma, int cg) {
     float Sx[32], gm[32];
-    ptx::tmem_ld32(x.lane_base + tm_s + 32 * x.cg, Sx);
-    const float *g = gamma + 32 * x.cg;
+    ptx::tmem_ld32(x.lane_base + tm_s + 32 * cg, Sx);
+    const float *g = gamma + 32 * cg;
     ld8(g, gm); ld8(g + 8, gm + 8); ld8(g + 16, gm + 16); ld8(g + 24, gm + 24);
     ptx::tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 32; ++i) Sx[i] *= gm[i];
-    ptx::tmem_st32(x.lane_base + tm_s + 32 * x.cg, Sx);
+    ptx::tmem_st32(x.lane_base + tm_s + 32 * cg, Sx);
     ptx::tmem_st_wait();
+}
+__device__ __forceinline__ void scale_state(const Ctx &x, uint32_t tm_s, const float *gamma) {
+    scale_state_cols(x, tm_s, gamma, x.cg);
 }
 // U^T out of TMEM into its bf16 operand tile.
 __device__ __forceinline__ void u_out(const Ctx &x, uint32_t tm_u, uint32_t off_ru) {
@@ -1603,9 +1606,18 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
             ptx::bulk_wait_read();   // the previous output tile has left RU
         }
         ++s_issued;
+        // the master state is not touched by that MMA: scale it meanwhile.  Warp 0
+        // is issuing, so warp 8 (the same TMEM lane quarter) scales its columns
+        // too; the block barrier after the scaling orders the previous output
+        // tile's read of RU before U is written there
+        ptx::tc_fence_after_sync();
+        {
+            const float *gamma = reinterpret_cast<const float *>(stg + REC_G);
+            if (warp != 0) scale_state(x, TS_D3, gamma);
+            if (warp == 8) scale_state_cols(x, TS_D3, gamma, 0);
+        }
+        ptx::tc_fence_before_sync();
         __syncthreads();
-        // the master state is not touched by that MMA: scale it meanwhile
-        scale_state(x, TS_D3, reinterpret_cast<const float *>(stg + REC_G));
         if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
         u_out(x, d1, SB_RU);
@@ -1850,10 +1862,17 @@ prefill_seg_kernel(const SplitParams p) {
             ptx::mma_commit(bar_s2);
         }
         ++s_issued;
-        // the two master states are not touched by those MMAs: scale them meanwhile
+        // the two master states are not touched by those MMAs: scale them meanwhile.
+        // Warps 0 and 1 are issuing, so warps 8 and 12 (lane quarter 0) and 9 and
+        // 13 (quarter 1) scale their columns of S0 and of M as well
         const float *gamma = reinterpret_cast<const float *>(stg + SG_G);
-        scale_state(x, TG_S, gamma);
-        scale_state(x, TG_M, gamma);
+        ptx::tc_fence_after_sync();
+        if (warp >= 2) {
+            scale_state(x, TG_S, gamma);
+            scale_state(x, TG_M, gamma);
+        }
+        if (warp == 8 || warp == 9) scale_state_cols(x, TG_S, gamma, 0);
+        if (warp == 12 || warp == 13) scale_state_cols(x, TG_M, gamma, 0);
         if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
         if (ptx::mbar_wait(bar_s2, s2_done & 1, kWaitBudget)) ++s2_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
