@@ -1486,17 +1486,26 @@ __device__ __forceinline__ void preload_u(const Ctx &x, uint32_t tm_d1, const ui
     ptx::tmem_st_wait();
 }
 
+// SPLIT: each record stage is refetched in two parts, each as soon as its own
+// readers are done (the windowed plan, whose records stream from DRAM);
+// otherwise whole after its chunk (the segment plans, whose records sit in L2).
+template <bool SPLIT>
 __global__ void __launch_bounds__(NT, 1)
 prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(sm);
-    uint64_t *bar_st = reinterpret_cast<uint64_t *>(sm + SB_BAR);   // [2] record stages
+    // A record stage arrives in two parts: [-W; Q~], U~^T and 2^G_end (read by the
+    // first product, the preload and the state scaling) and Kend^T and P (read
+    // by the state and output products), so that each part of a stage is
+    // refetched as soon as its own readers are done
+    uint64_t *bar_st = reinterpret_cast<uint64_t *>(sm + SB_BAR);   // [2] first parts of the stages
     uint64_t *bar_s = bar_st + 2;
     uint64_t *bar_m = bar_st + 3;      // the state update (thread 0)
     uint64_t *bar_m2 = bar_st + 4;     // the output product (thread 32: one thread issues a
                                        // tcgen05.mma only about every 100 cycles)
+    uint64_t *bar_kp = bar_st + 5;     // [2] second parts (Kend^T, P) of the stages
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + SB_BAR + 64);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + SB_BAR + 72);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1554,34 +1563,53 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     // this kernel is the last reader of the records: they are fetched with
     // evict_first and, once in shared memory, dropped from L2 without a write-back
     const uint64_t pol_rec = ptx::policy_evict_first();
-    auto fetch = [&](int k, int c) {
-        const uint8_t *r = recs + (size_t)(c - rec_c0) * REC_BYTES;
-        if (p.rec_in_l2) {
-            ptx::mbar_arrive_expect_tx(bar_st + k, REC_BYTES);
-            bulk_copy_in_hint(sm + k * SB_STAGE, r, REC_BYTES, bar_st + k, pol_rec);
-        } else {
-            bulk_load(sm + k * SB_STAGE, r, REC_BYTES, bar_st + k);
-        }
+    // byte ranges of the two parts in a record (and in its stage)
+    static_assert(REC_B1 == 0 && REC_KE == 32768 && REC_PB == REC_KE + 16384 && REC_UT == REC_PB + 8192 &&
+                  REC_G == REC_UT + 16384 && REC_BYTES == REC_G + 512, "record layout");
+    auto copy_part = [&](int k, const uint8_t *r, uint32_t off, uint32_t bytes, uint64_t *bar) {
+        if (p.rec_in_l2) bulk_copy_in_hint(sm + k * SB_STAGE + off, r + off, bytes, bar, pol_rec);
+        else bulk_copy_in(sm + k * SB_STAGE + off, r + off, bytes, bar);
     };
+    auto fetch_first = [&](int k, int c) {   // [-W; Q~], then U~^T and 2^G_end
+        const uint8_t *r = recs + (size_t)(c - rec_c0) * REC_BYTES;
+        ptx::mbar_arrive_expect_tx(bar_st + k, REC_KE + (REC_BYTES - REC_UT));
+        copy_part(k, r, REC_B1, REC_KE, bar_st + k);
+        copy_part(k, r, REC_UT, REC_BYTES - REC_UT, bar_st + k);
+    };
+    auto fetch_second = [&](int k, int c) {   // Kend^T and P
+        const uint8_t *r = recs + (size_t)(c - rec_c0) * REC_BYTES;
+        ptx::mbar_arrive_expect_tx(bar_kp + k, REC_UT - REC_KE);
+        copy_part(k, r, REC_KE, REC_UT - REC_KE, bar_kp + k);
+    };
+    constexpr bool split_fetch = SPLIT;
+    auto fetch_whole = [&](int k, int c) {
+        const uint8_t *r = recs + (size_t)(c - rec_c0) * REC_BYTES;
+        ptx::mbar_arrive_expect_tx(bar_st + k, REC_BYTES);
+        copy_part(k, r, 0, REC_BYTES, bar_st + k);
+    };
+    // (only once both parts of the record are in shared memory)
     auto discard = [&](int c) {
         if (!p.rec_in_l2) return;
         const uint8_t *r = recs + (size_t)(c - rec_c0) * REC_BYTES;
         for (int i = tid; i < (int)(REC_BYTES / 128); i += NT) ptx::discard_l2(r + (size_t)i * 128);
     };
 
-    uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0};
+    uint32_t st_issued[2] = {0, 0}, st_done[2] = {0, 0}, kp_issued[2] = {0, 0}, kp_done[2] = {0, 0};
     uint32_t s_issued = 0, s_done = 0, m_issued = 0, m_done = 0, m2_done = 0;
     const int c0 = w0;
     if (tid == 0) {
-        for (int k = 0; k < 2; ++k)
-            if (c0 + k < c_end) fetch(k, c0 + k);
+        for (int k = 0; k < 2; ++k) {
+            if (c0 + k >= c_end) continue;
+            if (split_fetch) { fetch_first(k, c0 + k); fetch_second(k, c0 + k); }
+            else fetch_whole(k, c0 + k);
+        }
     }
     for (int k = 0; k < 2; ++k)
-        if (c0 + k < c_end) ++st_issued[k];
+        if (c0 + k < c_end) { ++st_issued[k]; if (split_fetch) ++kp_issued[k]; }
     const float *src = first ? (p.initial_state ? p.initial_state + sidx : nullptr) : carried;
     load_state(x, src, TS_D3, SB_ST);
     if (c0 < c_end) {
-        if (ptx::mbar_wait(bar_st, st_done[0] & 1, kWaitBudget)) { ++st_done[0]; discard(c0); } else *s_abort = 1;
+        if (ptx::mbar_wait(bar_st, st_done[0] & 1, kWaitBudget)) ++st_done[0]; else *s_abort = 1;
         preload_u(x, TS_D1, sm + REC_UT);
     }
     if (test_wait_expires(p.test_expire, kExpireState, bar_never)) *s_abort = 1;
@@ -1621,6 +1649,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         if (ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done; else *s_abort = 1;
         ptx::tc_fence_after_sync();
         u_out(x, d1, SB_RU);
+        // this record's second part, fetched two chunks ago
+        if (split_fetch) {
+            if (ptx::mbar_wait(bar_kp + k, kp_done[k] & 1, kWaitBudget)) ++kp_done[k]; else *s_abort = 1;
+        }
         ptx::fence_async_smem();
         ptx::tc_fence_before_sync();
         __syncthreads();
@@ -1637,18 +1669,27 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
             ptx::mma_commit(bar_m2);
         }
         ++m_issued;
+        // the first part of stage k has been read (the first product, the scaling,
+        // the preload a chunk ago): the record two chunks ahead goes there now, from
+        // thread 0, whose warp has no share of the preload
+        if (split_fetch && c + 2 < c_end) {
+            if (tid == 0) fetch_first(k, c + 2);
+            ++st_issued[k];
+        }
+        discard(c);   // both parts of this record are in shared memory: its L2 lines go
         // meanwhile: the next chunk's [U~ | 0] into the other D1 buffer
         if (c + 1 < c_end) {
-            if (ptx::mbar_wait(bar_st + (k ^ 1), st_done[k ^ 1] & 1, kWaitBudget)) {
-                ++st_done[k ^ 1];
-                discard(c + 1);
-            } else {
-                *s_abort = 1;
-            }
+            if (ptx::mbar_wait(bar_st + (k ^ 1), st_done[k ^ 1] & 1, kWaitBudget)) ++st_done[k ^ 1];
+            else *s_abort = 1;
             preload_u(x, TS_D1 + 128 * (k ^ 1), sm + (k ^ 1) * SB_STAGE + REC_UT);
         }
         if (ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done; else *s_abort = 1;
         if (ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done; else *s_abort = 1;
+        // the second part of stage k has been read by those products
+        if (split_fetch && c + 2 < c_end) {
+            if (tid == 0) fetch_second(k, c + 2);
+            ++kp_issued[k];
+        }
         ptx::tc_fence_after_sync();
         phase_state_out(x, TS_D3, d1 + 64, SB_ST, SB_RU);
         ptx::fence_async_smem();
@@ -1656,9 +1697,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
         __syncthreads();
         if (*s_abort) break;
         store_output(x, &tm_o, SB_RU, p.out, row0, nvalid, hx, rowstride);
-        // stage k has been consumed: fetch the record two chunks ahead into it
-        if (tid == 0 && c + 2 < c_end) fetch(k, c + 2);
-        if (c + 2 < c_end) ++st_issued[k];
+        if (!split_fetch && c + 2 < c_end) {   // stage k has been consumed
+            if (tid == 0) fetch_whole(k, c + 2);
+            ++st_issued[k];
+        }
     }
     if (!*s_abort) {
         if (last) {
@@ -1670,8 +1712,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     __syncthreads();
     if (*s_abort) {
         if (tid == 0) report_status(p.status, kDevTimeout);
-        for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < 2; ++k) {
             while (st_done[k] < st_issued[k] && ptx::mbar_wait(bar_st + k, st_done[k] & 1, kWaitBudget)) ++st_done[k];
+            while (kp_done[k] < kp_issued[k] && ptx::mbar_wait(bar_kp + k, kp_done[k] & 1, kWaitBudget)) ++kp_done[k];
+        }
         while (s_done < s_issued && ptx::mbar_wait(bar_s, s_done & 1, kWaitBudget)) ++s_done;
         while (m_done < m_issued && ptx::mbar_wait(bar_m, m_done & 1, kWaitBudget)) ++m_done;
         while (m2_done < m_issued && ptx::mbar_wait(bar_m2, m2_done & 1, kWaitBudget)) ++m2_done;
@@ -2453,7 +2497,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
                           mg, mo, prm);
     }
     const void *kernels[4] = {(const void *)tc::prefill_intra_kernel<true>, (const void *)tc::prefill_seg_kernel,
-                              (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel};
+                              (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel<false>};
     const uint32_t smem[4] = {tc::SMEM_ALLOC, tc::SMEM_SEG, tc::SMEM_SCAN, tc::SMEM_STATE};
     for (int i = 0; i < 4; ++i)
         if ((e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2493,7 +2537,7 @@ cudaError_t launch_prefill_tc_logdecay(const void *q, const void *k, const void 
     if ((e = launch_pdl(tc::prefill_scan_kernel, (unsigned)(chains * tc::SCAN_SPLIT), tc::SCAN_NT,
                         tc::SMEM_SCAN, st, ms0, msin, sp)) != cudaSuccess)
         return e;
-    return launch_pdl(tc::prefill_state_kernel, cells, tc::NT, tc::SMEM_STATE, st, mo, sp);
+    return launch_pdl(tc::prefill_state_kernel<false>, cells, tc::NT, tc::SMEM_STATE, st, mo, sp);
 }
 
 // ---- segment maps (kda_segment_map) ------------------------------------------
@@ -2634,7 +2678,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const ScanPlan scan = plan_scan(total, num_seqs, H);
     if (scan.ok && workspace_bytes >= scan.bytes) {
         const void *kernels[4] = {(const void *)tc::prefill_intra_kernel<false>, (const void *)tc::prefill_seg_kernel,
-                                  (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel};
+                                  (const void *)tc::prefill_scan_kernel, (const void *)tc::prefill_state_kernel<false>};
         const uint32_t smem[4] = {tc::SMEM_ALLOC, tc::SMEM_SEG, tc::SMEM_SCAN, tc::SMEM_STATE};
         for (int i = 0; i < 4; ++i)
             if ((e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2671,7 +2715,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         if ((e = launch_pdl(tc::prefill_scan_kernel, (unsigned)(chains * tc::SCAN_SPLIT), tc::SCAN_NT,
                             tc::SMEM_SCAN, st, ms0, msin, sp)) != cudaSuccess)
             return e;
-        return launch_pdl(tc::prefill_state_kernel, cells, tc::NT, tc::SMEM_STATE, st, mo, sp);
+        return launch_pdl(tc::prefill_state_kernel<false>, cells, tc::NT, tc::SMEM_STATE, st, mo, sp);
     }
 
     const SplitPlan plan = plan_split(total, num_seqs, H);
@@ -2679,7 +2723,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         e = cudaFuncSetAttribute(tc::prefill_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)tc::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(tc::prefill_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(tc::prefill_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)tc::SMEM_STATE);
         if (e != cudaSuccess) return e;
         std::lock_guard<std::mutex> lock(g_side_mu);
@@ -2715,7 +2759,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             if ((e = cudaEventRecord(ss->intra[buf], ss->s)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(st, ss->intra[buf], 0)) != cudaSuccess) return e;
-            tc::prefill_state_kernel<<<(unsigned)chains, tc::NT, tc::SMEM_STATE, st>>>(mo, sp);
+            tc::prefill_state_kernel<true><<<(unsigned)chains, tc::NT, tc::SMEM_STATE, st>>>(mo, sp);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             if ((e = cudaEventRecord(ss->state[buf], st)) != cudaSuccess) return e;
         }
