@@ -1496,11 +1496,12 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_o, const SplitParams
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_addr(sm);
-    // A record stage arrives in two parts: [-W; Q~], U~^T and 2^G_end (read by the
-    // first product, the preload and the state scaling) and Kend^T and P (read
-    // by the state and output products), so that each part of a stage is
-    // refetched as soon as its own readers are done
-    uint64_t *bar_st = reinterpret_cast<uint64_t *>(sm + SB_BAR);   // [2] first parts of the stages
+    // With SPLIT a record stage arrives in two parts: [-W; Q~], U~^T and 2^G_end
+    // (read by the first product, the preload and the state scaling) on bar_st,
+    // Kend^T and P (read by the state and output products) on bar_kp, so that
+    // each part of a stage is refetched as soon as its own readers are done;
+    // otherwise the whole record arrives on bar_st
+    uint64_t *bar_st = reinterpret_cast<uint64_t *>(sm + SB_BAR);   // [2] per stage
     uint64_t *bar_s = bar_st + 2;
     uint64_t *bar_m = bar_st + 3;      // the state update (thread 0)
     uint64_t *bar_m2 = bar_st + 4;     // the output product (thread 32: one thread issues a
