@@ -18,14 +18,17 @@
 // the same section); each L and P entry is a sum of products k_tc k_sc
 // e^{G_tc - G_sc} with an exponent <= 0.
 //
-// One CTA of 256 threads per (sequence, head, block of 32 value channels);
-// thread (j = tid % 32, row group rg = tid / 32) keeps rows rg DK/8 ..
-// (rg + 1) DK/8 - 1 of state column j in registers.  Per chunk: stage the
-// inputs, cumulative decay and the four operand tiles (one thread per key
-// channel), L and P (one thread per (t, s) pair), the partial products K~ S0
-// and Q~ S0 over each row group, then the 16 x 16 forward substitution (one
-// warp) beside the reduction of those partials into V - K~ S0 and Q~ S0, then U,
-// then the output and the state update.
+// One CTA of 256 threads per (sequence, head, block of JB value channels), JB
+// = 32 when the batch gives at least two CTAs per SM, else 16 or 8 (more CTAs,
+// fewer state rows per thread; the state-independent work of a chunk is then
+// repeated per block); thread (j = tid % JB, row group rg = tid / JB) keeps
+// rows rg DK/RG .. (rg + 1) DK/RG - 1 of state column j in registers, RG =
+// 256 / JB.  Per chunk: stage the inputs (loaded into registers during the
+// previous chunk), cumulative decay and the four operand tiles (one thread per
+// key channel), L and P (one thread per (t, s) pair), the partial products
+// K~ S0 and Q~ S0 over each row group, then the 16 x 16 forward substitution
+// (one warp) beside the reduction of those partials into V - K~ S0 and Q~ S0,
+// then U, then the output and the state update.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -37,12 +40,11 @@ namespace chunk_simt {
 
 constexpr int C = 16;      // tokens per chunk (one 16-token decay tile)
 constexpr int NT = 256;    // threads per CTA
-constexpr int JB = 32;     // value channels per CTA
-constexpr int RG = NT / JB;   // row groups (8)
 
-template <int DK>
+template <int DK, int JB>
 struct Smem {
     static constexpr int PK = DK + 1;   // padded row: column reads of the tiles are conflict-free
+    static constexpr int RG = NT / JB;  // row groups
     float kt[C][PK], kh[C][PK], qt[C][PK], ke[C][PK];   // K~, K^, Q~, Kend (raw k, q, G while staging)
     float red[2][RG][C][JB + 1];                         // partial K~ S0 and Q~ S0 per row group
     float L[C][C + 1], P[C][C + 1], T[C][C + 1];
@@ -50,15 +52,19 @@ struct Smem {
     float eA[DK], gend[DK], beta[C];
 };
 
-template <typename T, int DK>
+template <typename T, int DK, int JB>
 __global__ void __launch_bounds__(NT) prefill_chunk_simt_kernel(
     const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v, const T *__restrict__ z,
     const float *__restrict__ A, const float *__restrict__ beta, const int32_t *__restrict__ cu_seqlens,
     int64_t total_tokens, int H, int dv, const float *__restrict__ initial_state,
     float *__restrict__ final_state, T *__restrict__ out, uint32_t *status) {
+    constexpr int RG = NT / JB;    // row groups
     constexpr int RPT = DK / RG;   // state rows per thread
+    static_assert(NT % JB == 0 && DK % RG == 0 && RPT >= 1, "value block");
+    constexpr int KE = C * DK / NT;                 // staged k, q, z elements per thread
+    constexpr int VE = (C * JB + NT - 1) / NT;      // staged v elements per thread
     extern __shared__ float4 smem_f4[];
-    Smem<DK> &sm = *reinterpret_cast<Smem<DK> *>(smem_f4);
+    Smem<DK, JB> &sm = *reinterpret_cast<Smem<DK, JB> *>(smem_f4);
 
     const int sh = blockIdx.x;
     const int seq = sh / H, h = sh % H;
@@ -79,28 +85,50 @@ __global__ void __launch_bounds__(NT) prefill_chunk_simt_kernel(
         S[i] = initial_state ? initial_state[sbase + (int64_t)(c0 + i) * dv + j0 + j] : 0.f;
     for (int c = tid; c < DK; c += NT) sm.eA[c] = expf(A[h * DK + c]);
 
+    // this thread's raw inputs of a chunk (element e = tid + NT i of the [C][DK]
+    // and [C][JB] tiles; rows past the sequence end read as zero), loaded one
+    // chunk ahead so that their latency is spent under the previous chunk
+    float rk[KE], rq[KE], rz[KE], rv[VE], rb = 0.f;
+    auto load_raw = [&](int64_t ta) {
+        const int na = (int)((eos - ta) < C ? (eos - ta) : C);
+#pragma unroll
+        for (int i = 0; i < KE; ++i) {
+            const int e = tid + NT * i, t = e / DK, c = e % DK;
+            rk[i] = rq[i] = rz[i] = 0.f;
+            if (t < na) {
+                const int64_t idx = ((ta + t) * H + h) * DK + c;
+                rk[i] = to_f32(k[idx]);
+                rq[i] = to_f32(q[idx]);
+                rz[i] = to_f32(z[idx]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VE; ++i) {
+            const int e = tid + NT * i, t = e / JB, jj = e % JB;
+            rv[i] = (e < C * JB && t < na) ? to_f32(v[((ta + t) * H + h) * (int64_t)dv + j0 + jj]) : 0.f;
+        }
+        rb = (tid < na) ? beta[(ta + tid) * H + h] : 0.f;
+    };
+    if (bos < eos) load_raw(bos);
+
     for (int64_t t0 = bos; t0 < eos; t0 += C) {
         const int nt = (int)((eos - t0) < C ? (eos - t0) : C);
         __syncthreads();   // the previous chunk is consumed (and eA is ready)
         // ---- stage: raw k and q, the gate's log-decay g (rows >= nt: zeros), v, beta
-        for (int e = tid; e < C * DK; e += NT) {
-            const int t = e / DK, c = e % DK;
-            float kk = 0.f, qq = 0.f, gg = 0.f;
-            if (t < nt) {
-                const int64_t idx = ((t0 + t) * H + h) * DK + c;
-                kk = to_f32(k[idx]);
-                qq = to_f32(q[idx]);
-                gg = gate_log_decay(sm.eA[c], to_f32(z[idx]));
-            }
-            sm.kh[t][c] = kk;
-            sm.qt[t][c] = qq;
-            sm.ke[t][c] = gg;
+#pragma unroll
+        for (int i = 0; i < KE; ++i) {
+            const int e = tid + NT * i, t = e / DK, c = e % DK;
+            sm.kh[t][c] = rk[i];
+            sm.qt[t][c] = rq[i];
+            sm.ke[t][c] = t < nt ? gate_log_decay(sm.eA[c], rz[i]) : 0.f;
         }
-        for (int e = tid; e < C * JB; e += NT) {
-            const int t = e / JB, jj = e % JB;
-            sm.v[t][jj] = t < nt ? to_f32(v[((t0 + t) * H + h) * (int64_t)dv + j0 + jj]) : 0.f;
+#pragma unroll
+        for (int i = 0; i < VE; ++i) {
+            const int e = tid + NT * i;
+            if (e < C * JB) sm.v[e / JB][e % JB] = rv[i];
         }
-        if (tid < C) sm.beta[tid] = tid < nt ? beta[(t0 + tid) * H + h] : 0.f;
+        if (tid < C) sm.beta[tid] = rb;
+        if (t0 + C < eos) load_raw(t0 + C);   // the next chunk's inputs, in flight meanwhile
         __syncthreads();
         // ---- cumulative decay and the operand tiles, one thread per key channel
         for (int c = tid; c < DK; c += NT) {
@@ -223,19 +251,37 @@ __global__ void __launch_bounds__(NT) prefill_chunk_simt_kernel(
     }
 }
 
+template <typename T, int DK, int JB>
+cudaError_t launch_jb(const void *q, const void *k, const void *v, const void *z, const float *A,
+                      const float *beta, const int32_t *cu, int num_seqs, int64_t total, int H, int dv,
+                      const float *s0, float *s1, void *out, uint32_t *status, cudaStream_t st) {
+    const size_t smem = sizeof(Smem<DK, JB>);
+    cudaError_t e = cudaFuncSetAttribute(prefill_chunk_simt_kernel<T, DK, JB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((int64_t)num_seqs * H), (unsigned)(dv / JB));
+    prefill_chunk_simt_kernel<T, DK, JB><<<grid, NT, smem, st>>>(
+        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
+        static_cast<const T *>(z), A, beta, cu, total, H, dv, s0, s1, static_cast<T *>(out), status);
+    return cudaGetLastError();
+}
+
+// The value block: 32 channels when the batch gives at least two CTAs per SM,
+// else 16 or 8 (each chain's chunks run one after another whatever the block,
+// so a narrow block only adds CTAs and shortens each chunk's state work).
 template <typename T, int DK>
 cudaError_t launch_dk(const void *q, const void *k, const void *v, const void *z, const float *A,
                       const float *beta, const int32_t *cu, int num_seqs, int64_t total, int H, int dv,
                       const float *s0, float *s1, void *out, uint32_t *status, cudaStream_t st) {
-    const size_t smem = sizeof(Smem<DK>);
-    cudaError_t e = cudaFuncSetAttribute(prefill_chunk_simt_kernel<T, DK>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((int64_t)num_seqs * H), (unsigned)(dv / JB));
-    prefill_chunk_simt_kernel<T, DK><<<grid, NT, smem, st>>>(
-        static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v),
-        static_cast<const T *>(z), A, beta, cu, total, H, dv, s0, s1, static_cast<T *>(out), status);
-    return cudaGetLastError();
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t chains = (int64_t)num_seqs * H;
+    if (chains * (dv / 32) >= 2 * (int64_t)sms)
+        return launch_jb<T, DK, 32>(q, k, v, z, A, beta, cu, num_seqs, total, H, dv, s0, s1, out, status, st);
+    if (chains * (dv / 16) >= 2 * (int64_t)sms)
+        return launch_jb<T, DK, 16>(q, k, v, z, A, beta, cu, num_seqs, total, H, dv, s0, s1, out, status, st);
+    return launch_jb<T, DK, 8>(q, k, v, z, A, beta, cu, num_seqs, total, H, dv, s0, s1, out, status, st);
 }
 
 }  // namespace chunk_simt
@@ -248,7 +294,7 @@ cudaError_t launch_prefill_chunk_simt(const void *q, const void *k, const void *
                                       float *s1, void *out, uint32_t *status, cudaStream_t st) {
     using namespace chunk_simt;
     if (num_seqs <= 0) return cudaSuccess;
-    if (dv % JB != 0) return cudaErrorInvalidValue;
+    if (dv % 32 != 0) return cudaErrorInvalidValue;
 #define KDA_CHUNK_SIMT_CASE(TT, DKK)                                                                       \
     return launch_dk<TT, DKK>(q, k, v, z, A, beta, cu, num_seqs, total, H, dv, s0, s1, out, status, st)
     if (bf16) {

@@ -106,6 +106,25 @@ def test_chunked_float32_path_long_sequences(dtype, dk, dv, slow):
     assert_close("final state", fin, rf, dtype)
 
 
+@pytest.mark.parametrize("n_seqs,dtype,dk,dv", [(160, torch.float32, 32, 32), (100, torch.float32, 32, 32),
+                                                 (8, torch.bfloat16, 64, 64)])
+def test_chunked_float32_path_value_blocks(n_seqs, dtype, dk, dv):
+    """The chunkwise float32 kernel's value blocks: 32 channels per CTA when a
+    batch gives at least two CTAs per SM, else 16 or 8 (on a 152-SM GPU: 320
+    chains of 32 channels take the 32-channel block, 200 the 16-channel one,
+    16 chains of 64 the 8-channel one).  Ragged lengths, a random start state,
+    against the oracle."""
+    dev = need_gpu()
+    rng = np.random.default_rng(23 + n_seqs)
+    lens = [int(x) for x in rng.integers(1, 60, n_seqs)]
+    w = inputs.custom(lens, H=2, dk=dk, dv=dv, dtype=dtype, init="randn0.1", wid=23)
+    d = inputs.prefill_inputs(w)
+    out, fin = _run_gpu(d, dev)
+    ro, rf = _run_oracle(d)
+    assert_close("out", out, ro, dtype)
+    assert_close("final state", fin, rf, dtype)
+
+
 def test_null_final_state_and_in_place_state():
     dev = need_gpu()
     w = inputs.custom([300, 77], H=2, dk=128, dv=128, dtype=torch.bfloat16, init="randn0.1", wid=12)
