@@ -249,7 +249,7 @@ def test_householder_product_form_matches():
     np.testing.assert_allclose(fin, hf, rtol=1e-11, atol=1e-12)
 
 
-@pytest.mark.parametrize("C", [1, 4, 16, 64])
+@pytest.mark.parametrize("C", [1, 4, 7, 16, 32, 64])   # 16, 32, 64: the chunk sizes of the GPU kernels
 def test_chunked_wy_form_matches(C):
     rng = np.random.default_rng(6 + C)
     p = _rand_problem(rng, [70, 17, 1, 33], 2, 8, 6)
